@@ -1,0 +1,516 @@
+#!/usr/bin/env python3
+"""Benchmark of the DBuffer group-operator pass on GB300.
+
+One step = one pass of every group operator over every DBuffer of the 7B-shaped
+dense stack (32 transformer layers d=4096 ffn=11008 + the 32000x4096 embedding,
+one DBuffer per layer, m=64 shard slices, 128x128 blocks, E4M3 128x128 block
+quantisation, s = 1/64): per DBuffer
+  pack_cast  fp32 master params -> bf16 flat buffer      (6 B/elem)
+  unpack     bf16 flat buffer -> bf16 compute tensors    (4 B/elem)
+  scale_accum_zero  fp32 grads -> fp32 accumulator       (16 B/elem)
+  norm_nonfinite    fp32 accumulator                     (4 B/elem)
+  block_quant       fp32 accumulator -> E4M3 codes       (5 B/elem + 4 B/block)
+Throughput = algorithmic bytes (tensor ranges only, padding excluded) / time.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+N>1 runs under torch.distributed.run: one independent replica per GPU (the path
+has no exchange step on one GPU), timing max over ranks.  --impl reference times
+the CPU oracle on a bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+METRIC = "fused group-op HBM GB/s (fraction of GB300 peak); params/sec per buffer pass"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+REF_SAMPLE_ROWS = 8000  # rows of the embedding table in the CPU sample
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device):
+        self.uuid = None
+        try:
+            self.uuid = str(torch.cuda.get_device_properties(device).uuid)
+        except Exception:
+            pass
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                p = [x.strip() for x in line.split(",")]
+                if len(p) < 9:
+                    continue
+                if self.uuid and self.uuid.replace("GPU-", "") not in p[0]:
+                    continue
+                rows.append(p)
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in rows if num(r[1]) is not None]
+        mx = [num(r[2]) for r in rows if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        load = [s for s in sm if mx and s >= 0.5 * max(mx)] or sm
+        return {"sm_mhz": statistics.median(load) if load else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ---------------------------------------------------------------------------
+# workload: every DBuffer of the 7B-shaped stack
+# ---------------------------------------------------------------------------
+OP_BYTES = {"pack_cast": 6, "unpack": 4, "scale_accum_zero": 16, "norm_nonfinite": 4}
+
+
+class Stack:
+    """Plans, user tensors and flat buffers of the dense stack on one GPU.  The
+    32 layer DBuffers share one plan and one set of flat buffers (the buffers are
+    the padded m*S layout, 7.5x a layer, so one set is reused layer by layer);
+    each DBuffer keeps its own user tensors."""
+
+    def __init__(self, w, device, layers=None):
+        from fsdp_infra_gb300 import DBuffer
+        from workloads import param_values
+        self.w = w
+        self.device = device
+        self.groups = []  # (group index, DBuffer, count)
+        self.dbufs = []
+        for gi, g in enumerate(w.groups):
+            db = DBuffer(g.tensors, w.m, w.local_units, w.align, device=device).upload()
+            kind = {"db": db, "gi": gi, "spec": g,
+                    "buf16": torch.zeros(db.total, dtype=torch.bfloat16, device=device),
+                    "grad": torch.zeros(db.total, dtype=w.grad_dtype, device=device),
+                    "acc": torch.zeros(db.total, dtype=torch.float32, device=device),
+                    "codes": torch.zeros(db.total, dtype=torch.uint8, device=device),
+                    "scales": torch.zeros(max(db.n_scales, 1), dtype=torch.float32, device=device)}
+            gen = torch.Generator(device=device)
+            gen.manual_seed(1234 + gi)
+            for t, s in enumerate(g.tensors):
+                o = db.offsets[t]
+                kind["grad"][o:o + s.numel].normal_(0.0, w.grad_std, generator=gen)
+            reps = g.repeat if layers is None else min(g.repeat, layers)
+            for r in range(reps):
+                params = [param_values(w, gi, t, device=device, seed=1000 * r + gi)
+                          for t in range(len(g.tensors))]
+                compute = [torch.empty(s.rows, s.cols, dtype=torch.bfloat16, device=device)
+                           for s in g.tensors]
+                out = (torch.empty(len(g.tensors), dtype=torch.float32, device=device),
+                       torch.empty(1, dtype=torch.float32, device=device),
+                       torch.empty(1, dtype=torch.int32, device=device))
+                db.ptr_table(params)
+                db.ptr_table(compute)
+                self.dbufs.append({"kind": kind, "params": params, "compute": compute,
+                                   "out": out})
+        self.elements = sum(g.numel * (g.repeat if layers is None else min(g.repeat, layers))
+                            for g in w.groups)
+        self.op_bytes = {k: v * self.elements for k, v in OP_BYTES.items()}
+        qe, ns = 0, 0
+        for d in self.dbufs:
+            k = d["kind"]
+            qe += sum(s.numel for s in k["spec"].tensors if s.quant)
+            ns += k["db"].n_scales
+        self.op_bytes["block_quant"] = 5 * qe + 4 * ns
+        self.bytes_per_step = sum(self.op_bytes.values())
+        self.launches_per_step = 6 * len(self.dbufs)  # pack, unpack, sac, norm x2, quant
+
+    def step(self, timers=None):
+        w = self.w
+        for d in self.dbufs:
+            k, db = d["kind"], d["kind"]["db"]
+            if timers:
+                timers.mark("pack_cast", 0)
+            db.pack_cast(d["params"], k["buf16"])
+            if timers:
+                timers.mark("pack_cast", 1); timers.mark("unpack", 0)
+            db.unpack(k["buf16"], d["compute"])
+            if timers:
+                timers.mark("unpack", 1); timers.mark("scale_accum_zero", 0)
+            db.scale_accum_zero(k["grad"], k["acc"], w.scale)
+            if timers:
+                timers.mark("scale_accum_zero", 1); timers.mark("norm_nonfinite", 0)
+            db.norm_nonfinite(k["acc"], out=d["out"])
+            if timers:
+                timers.mark("norm_nonfinite", 1); timers.mark("block_quant", 0)
+            db.block_quant(k["acc"], codes=k["codes"], scales=k["scales"])
+            if timers:
+                timers.mark("block_quant", 1)
+
+
+class OpTimers:
+    """CUDA events around every operator launch on the launching stream."""
+
+    def __init__(self):
+        self.events = {}
+
+    def mark(self, op, which):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record(torch.cuda.current_stream())
+        self.events.setdefault(op, [[], []])[which].append(e)
+
+    def totals_ms(self):
+        out = {}
+        for op, (s, e) in self.events.items():
+            out[op] = [a.elapsed_time(b) for a, b in zip(s, e)]
+        return out
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle on a bounded sample (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+def oracle_sample_pass(reps=1):
+    """Times the oracle (single-threaded C) on a slice of the embedding table
+    planned as its own DBuffer (m=64, 128x128 blocks, E4M3): all five operators.
+    Returns (GB/s, elements/s, seconds, description)."""
+    import numpy as np
+    import oracle
+    from workloads import workload
+    from workloads.configs import TensorSpec
+    w = workload("dense7b")
+    emb = w.groups[1].tensors[0]
+    spec = TensorSpec("embedding_rows", REF_SAMPLE_ROWS, emb.cols, emb.gran_rows, emb.qblock,
+                      emb.quant)
+    p = oracle.plan_specs([spec], w.m, None, w.align)
+    n = spec.numel
+    gen = torch.Generator().manual_seed(0)
+    src = (torch.randn(n, generator=gen) * 0.02).numpy()
+    grad = np.zeros(p.total, np.float32)
+    grad[p.offsets[0]:p.offsets[0] + n] = (torch.randn(n, generator=gen) * 1e-3).numpy()
+    acc = np.zeros(p.total, np.float32)
+    b16 = np.zeros(p.total, np.uint16)
+    dst = np.zeros(n, np.uint16)
+    codes = np.zeros(p.total, np.uint8)
+    _, ns = oracle.scale_offsets([spec])
+    nbytes = (6 + 4 + 16 + 4 + 5) * n + 4 * ns
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        oracle.pack(p, [src], b16)
+        oracle.unpack(p, b16, [dst])
+        oracle.scale_accum_zero(p, grad, acc, w.scale)
+        oracle.norm_nonfinite(p, acc)
+        oracle.block_quant(p, [spec], acc, codes)
+    dt = time.perf_counter() - t0
+    desc = (f"{REF_SAMPLE_ROWS}x{emb.cols} slice of the embedding table as one DBuffer "
+            f"(m={w.m}, {n} elements), all five operators, x{reps}")
+    return nbytes * reps / dt / 1e9, n * reps / dt, dt, desc
+
+
+def run_reference(args):
+    rank, world, local = _dist()
+    if rank != 0:
+        return 0
+    from oracle import build as build_oracle
+    build_oracle()
+    for _ in range(args.warmup):
+        oracle_sample_pass(1)
+    t0 = time.perf_counter()
+    gbs_l = []
+    for _ in range(args.steps):
+        gbs, eps, dt, desc = oracle_sample_pass(1)
+        gbs_l.append(gbs)
+    total = time.perf_counter() - t0
+    value = statistics.median(gbs_l)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(1000 * total / args.steps, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": _config_dict(None),
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def _config_dict(stack):
+    d = {"workload": "7B-shaped dense stack: 32 layers d=4096 ffn=11008 (Wqkv 4096x12288, "
+                     "Wo 4096x4096, gate/up 4096x11008, down 11008x4096, 2 norms) + embedding "
+                     "32000x4096; one DBuffer per layer, m=64, 128x128 blocks, E4M3 128x128 "
+                     "block quant, s=1/64",
+         "dbuffers": 33, "m": 64,
+         "ops_per_dbuffer": ["pack_cast f32->bf16", "unpack bf16->bf16",
+                             "scale_accum_zero f32", "norm_nonfinite f32", "block_quant e4m3"],
+         "l2": "inputs larger than L2: each DBuffer's tensor ranges are 0.52-0.81 GB, "
+               "L2 is 129 MB"}
+    if stack is not None:
+        d["elements_per_step"] = stack.elements
+        d["bytes_per_step"] = stack.bytes_per_step
+    return d
+
+
+def _traffic_for(kernel_key):
+    """dram bytes per launch recorded from an ncu capture, if the kernel source
+    is unchanged since (profiles/dram_traffic.txt carries the source hash)."""
+    path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    if not os.path.exists(path):
+        return None
+    src = {}
+    for f in os.listdir(os.path.join(ROOT, "fsdp_infra_gb300", "csrc")):
+        if f.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(ROOT, "fsdp_infra_gb300", "csrc", f), "rb") as fh:
+                src[f] = hashlib.sha256(fh.read()).hexdigest()[:16]
+    with open(path) as f:
+        for line in f:
+            if line.startswith("#") or "=" not in line:
+                continue
+            kv = dict(x.split("=", 1) for x in line.split())
+            if kv.get("op") != kernel_key:
+                continue
+            if src.get(kv.get("file")) != kv.get("sha"):
+                return None
+            return float(kv["bytes_per_launch"])
+    return None
+
+
+def run_ours(args):
+    rank, world, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    device = torch.device("cuda", torch.cuda.current_device())
+    from fsdp_infra_gb300 import build as _b  # noqa: F401  (library must already be built)
+    from workloads import workload
+    w = workload("dense7b")
+    stack = Stack(w, device)
+    torch.cuda.synchronize()
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    for _ in range(max(args.warmup, 0)):
+        stack.step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(device)
+    timers = OpTimers()
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    t_start = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_start.record()
+    for _ in range(args.steps):
+        stack.step(timers)
+    t_end.record()
+    torch.cuda.synchronize()
+    barrier()
+    clock_info = clocks.stop()
+    elapsed_ms = t_start.elapsed_time(t_end)
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([elapsed_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        elapsed_ms = float(t.item())
+    ms_per_step = elapsed_ms / args.steps
+    value = world * stack.bytes_per_step / (ms_per_step / 1e3) / 1e9
+
+    per_op = timers.totals_ms()
+    peak, peak_kind = _peaks()
+    ops = {}
+    for op, durs in per_op.items():
+        per_launch_bytes = stack.op_bytes[op] / len(stack.dbufs)
+        mean_ms = statistics.mean(durs)
+        ops[op] = {"ms_per_step": round(sum(durs) / args.steps, 4),
+                   "mean_launch_ms": round(mean_ms, 4),
+                   "gbs": round(stack.op_bytes[op] / (sum(durs) / args.steps / 1e3) / 1e9, 1),
+                   "frac": round(stack.op_bytes[op] / (sum(durs) / args.steps / 1e3) / 1e9 / peak, 4)}
+    dom = max(per_op, key=lambda k: sum(per_op[k]))
+    # achieved for the dominant operator: bytes of one launch on one layer DBuffer
+    # (the 32 layer launches dominate) over the mean layer-launch duration.
+    layer_db = stack.dbufs[0]["kind"]["db"]
+    layer_elems = stack.w.groups[0].numel
+    if dom == "block_quant":
+        layer_bytes = 5 * sum(s.numel for s in stack.w.groups[0].tensors if s.quant) + 4 * layer_db.n_scales
+    else:
+        layer_bytes = OP_BYTES[dom] * layer_elems
+    n_layers = stack.w.groups[0].repeat
+    layer_durs = [d for i, d in enumerate(per_op[dom]) if (i % len(stack.dbufs)) < n_layers]
+    mean_layer_ms = statistics.mean(layer_durs)
+    achieved = layer_bytes / (mean_layer_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
+                "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
+                "bytes_per_launch": layer_bytes,
+                "traffic": _traffic_for(dom)}
+
+    # ---- end to end: host inputs (pinned) -> device, operators, results -> host
+    e2e = run_e2e(stack, args, world)
+
+    line = None
+    if rank == 0:
+        cpu = None
+        if world == 1 and not args.no_cpu_baseline:
+            import oracle
+            oracle.build()
+            gbs, eps, dt, desc = oracle_sample_pass(1)
+            cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                   "sample": desc, "seconds": round(dt, 2)}
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+                "config": _config_dict(stack),
+                "params_per_s": round(world * stack.elements / (ms_per_step / 1e3), 1),
+                "frac_of_peak": round(value / world / peak, 4), "peak_kind": peak_kind,
+                "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+                "gpu_launches": stack.launches_per_step * args.steps,
+                "clocks": clock_info, "ops": ops}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def run_e2e(stack, args, world):
+    """Same step through the public API, with this step's inputs copied from
+    pinned host memory (fp32 master params and fp32 gradients of every DBuffer)
+    and the results (norms, non-finite flags) read back to the host."""
+    device = stack.device
+    host = {}
+    for d in stack.dbufs:
+        k = d["kind"]
+        if id(k) in host:
+            continue
+        g = k["spec"]
+        db = k["db"]
+        hp = [torch.empty(s.numel, dtype=torch.float32, pin_memory=True) for s in g.tensors]
+        hg = [torch.empty(s.numel, dtype=stack.w.grad_dtype, pin_memory=True) for s in g.tensors]
+        for t, s in enumerate(g.tensors):
+            hp[t].copy_(d["params"][t].reshape(-1))
+            hg[t].copy_(k["grad"][db.offsets[t]:db.offsets[t] + s.numel])
+        host[id(k)] = (hp, hg, torch.empty(len(g.tensors) + 2, dtype=torch.float32,
+                                           pin_memory=True))
+    h2d = 0
+    d2h = 0
+    for d in stack.dbufs:
+        hp, hg, _ = host[id(d["kind"])]
+        h2d += sum(x.numel() * x.element_size() for x in hp) + sum(x.numel() * x.element_size() for x in hg)
+        d2h += (len(hp) + 2) * 4
+
+    def step():
+        for d in stack.dbufs:
+            k, db = d["kind"], d["kind"]["db"]
+            hp, hg, hout = host[id(k)]
+            for t in range(len(hp)):
+                d["params"][t].view(-1).copy_(hp[t], non_blocking=True)
+                o = db.offsets[t]
+                k["grad"][o:o + hg[t].numel()].copy_(hg[t], non_blocking=True)
+            db.pack_cast(d["params"], k["buf16"])
+            db.unpack(k["buf16"], d["compute"])
+            db.scale_accum_zero(k["grad"], k["acc"], stack.w.scale)
+            norms, tot, flag = db.norm_nonfinite(k["acc"], out=d["out"])
+            db.block_quant(k["acc"], codes=k["codes"], scales=k["scales"])
+            n = len(hp)
+            hout[:n].copy_(norms, non_blocking=True)
+            hout[n:n + 1].copy_(tot, non_blocking=True)
+            hout[n + 1:n + 2].copy_(flag.view(torch.float32), non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+
+    for _ in range(max(1, min(args.warmup, 2))):
+        step()
+    steps = max(1, min(args.steps, 5))
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        step()
+    torch.cuda.synchronize()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([dt], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        dt = float(t.item())
+    value = world * stack.bytes_per_step * steps / dt / 1e9
+    return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+            "d2h_bytes_per_step": d2h, "steps": steps,
+            "ms_per_step": round(1000 * dt / steps, 3)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,154 @@
+// C ABI entry points of libdbuf: argument checks (synchronous, before any launch),
+// descriptor-table upload, and dispatch to the group-operator launchers.
+#include <cuda_runtime.h>
+
+#include <cstring>
+
+#include "dbuf_internal.h"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+    g_last_cuda_error = int(e);
+    return DBUF_ECUDA;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+bool dtype_ok(int32_t dt) { return dt == DBUF_F32 || dt == DBUF_BF16; }
+
+// Common checks of every operator: plan uploaded, device current.
+int check_plan(const dbuf_plan_t *p) {
+    if (!p) return DBUF_EINVAL;
+    if (!p->uploaded) return DBUF_ENOTUPLOADED;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (dev != p->dev.device) return DBUF_EDEVICE;
+    return DBUF_OK;
+}
+
+int finish(int e) { return e == cudaSuccess ? DBUF_OK : cuda_fail(cudaError_t(e)); }
+
+}  // namespace
+
+extern "C" int dbuf_last_cuda_error(void) { return g_last_cuda_error; }
+
+extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
+    if (!p) return DBUF_EINVAL;
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (p->uploaded) return dev == p->dev.device ? DBUF_OK : DBUF_EDEVICE;
+
+    const size_t b_t = align256(sizeof(dbuf::TensorDesc) * p->tdesc.size());
+    const size_t b_c = align256(sizeof(dbuf::Chunk) * p->chunks.size());
+    const size_t b_r = align256(sizeof(dbuf::QItem) * p->row_items.size());
+    const size_t b_q = align256(sizeof(dbuf::QItem) * p->tile_items.size());
+    const size_t bytes = b_t + b_c + b_r + b_q + 256;
+    void *base = nullptr;
+    e = cudaMalloc(&base, bytes);
+    if (e != cudaSuccess) {
+        (void)cudaGetLastError();
+        return e == cudaErrorMemoryAllocation ? DBUF_ENOMEM : cuda_fail(e);
+    }
+    char *c = static_cast<char *>(base);
+    dbuf::DeviceTables t;
+    t.base = base;
+    t.bytes = bytes;
+    t.device = dev;
+    t.tensors = reinterpret_cast<dbuf::TensorDesc *>(c);
+    t.chunks = reinterpret_cast<dbuf::Chunk *>(c + b_t);
+    t.row_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c);
+    t.tile_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c + b_r);
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    struct Piece {
+        void *dst;
+        const void *src;
+        size_t n;
+    } pieces[4] = {
+        {t.tensors, p->tdesc.data(), sizeof(dbuf::TensorDesc) * p->tdesc.size()},
+        {t.chunks, p->chunks.data(), sizeof(dbuf::Chunk) * p->chunks.size()},
+        {t.row_items, p->row_items.data(), sizeof(dbuf::QItem) * p->row_items.size()},
+        {t.tile_items, p->tile_items.data(), sizeof(dbuf::QItem) * p->tile_items.size()},
+    };
+    for (const Piece &pc : pieces) {
+        if (!pc.n) continue;
+        e = cudaMemcpyAsync(pc.dst, pc.src, pc.n, cudaMemcpyHostToDevice, st);
+        if (e != cudaSuccess) {
+            cudaFree(base);
+            return cuda_fail(e);
+        }
+    }
+    e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) {
+        cudaFree(base);
+        return cuda_fail(e);
+    }
+    p->dev = t;
+    p->uploaded = true;
+    return DBUF_OK;
+}
+
+extern "C" void dbuf_plan_free(dbuf_plan_t *p) {
+    if (!p) return;
+    if (p->uploaded && p->dev.base) {
+        int cur = -1;
+        cudaGetDevice(&cur);
+        if (cur != p->dev.device) cudaSetDevice(p->dev.device);
+        cudaFree(p->dev.base);
+        if (cur != p->dev.device && cur >= 0) cudaSetDevice(cur);
+    }
+    delete p;
+}
+
+extern "C" int dbuf_pack_cast(const dbuf_plan_t *p, const void *const *src, int32_t src_dtype,
+                              void *buf, int32_t buf_dtype, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(src_dtype) || !dtype_ok(buf_dtype)) return DBUF_EINVAL;
+    if (p->n > 0 && (!src || !buf)) return DBUF_EINVAL;
+    return finish(dbuf::launch_pack(p, src, src_dtype, buf, buf_dtype, stream));
+}
+
+extern "C" int dbuf_unpack(const dbuf_plan_t *p, const void *buf, int32_t buf_dtype,
+                           void *const *dst, int32_t dst_dtype, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(buf_dtype) || !dtype_ok(dst_dtype)) return DBUF_EINVAL;
+    if (p->n > 0 && (!dst || !buf)) return DBUF_EINVAL;
+    return finish(dbuf::launch_unpack(p, buf, buf_dtype, dst, dst_dtype, stream));
+}
+
+extern "C" int dbuf_scale_accum_zero(const dbuf_plan_t *p, void *grad, int32_t grad_dtype,
+                                     float *acc, float scale, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(grad_dtype)) return DBUF_EINVAL;
+    if (p->n > 0 && (!grad || !acc)) return DBUF_EINVAL;
+    return finish(dbuf::launch_sac(p, grad, grad_dtype, acc, scale, stream));
+}
+
+extern "C" int dbuf_norm_nonfinite(const dbuf_plan_t *p, const void *buf, int32_t dtype,
+                                   float *tensor_norms, float *total_norm, int32_t *nonfinite,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(dtype)) return DBUF_EINVAL;
+    if (!total_norm || !nonfinite || !workspace) return DBUF_EINVAL;
+    if (p->n > 0 && (!buf || !tensor_norms)) return DBUF_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DBUF_EINVAL;
+    if (workspace_bytes < dbuf::norm_workspace_bytes(p)) return DBUF_EINVAL;
+    return finish(dbuf::launch_norm(p, buf, dtype, tensor_norms, total_norm, nonfinite, workspace,
+                                    stream));
+}
+
+extern "C" int dbuf_block_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes,
+                                float *scales, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (p->n_scales > 0 && (!buf || !codes || !scales)) return DBUF_EINVAL;
+    return finish(dbuf::launch_quant(p, buf, codes, scales, stream));
+}

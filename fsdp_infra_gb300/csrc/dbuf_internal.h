@@ -1,0 +1,102 @@
+// Internal layout of a plan and of its device descriptor tables.
+// Shared by the host planner (planner.cpp) and the CUDA operators (*.cu).
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include "../../include/dbuf.h"
+
+namespace dbuf {
+
+// Elements per chunk of the elementwise operators.  A chunk never spans two
+// tensors, so every chunk has one source and one destination range; chunk
+// starts are multiples of kChunkElems inside a tensor.
+constexpr int64_t kChunkElems = 16384;
+
+// Blocks per work item of the row-block (1 x qc) quantisation kernel.
+constexpr int32_t kRowItemBlocks = 32;
+
+// One tensor of the group, as the kernels see it (64 bytes).
+struct TensorDesc {
+    int64_t buf_off;    // l_t
+    int64_t numel;      // n_t
+    int64_t rows;
+    int64_t cols;
+    int64_t scale_off;  // first block scale of this tensor
+    int32_t qrows;      // effective quantisation block rows (>= 1)
+    int32_t qcols;      // effective quantisation block cols (>= 1)
+    int32_t quant;      // DBUF_QUANT_*
+    int32_t nbc;        // quantisation blocks per block-row
+    int32_t chunk_begin;
+    int32_t chunk_end;
+};
+static_assert(sizeof(TensorDesc) == 64, "TensorDesc layout");
+
+// A contiguous piece of one tensor: elements [off, off+len) of tensor `tensor`.
+struct Chunk {
+    int64_t off;
+    int32_t tensor;
+    int32_t len;
+};
+static_assert(sizeof(Chunk) == 16, "Chunk layout");
+
+// A run of `count` consecutive quantisation blocks (row-major block order) of
+// one tensor, starting at block `first`.
+struct QItem {
+    int64_t first;
+    int32_t tensor;
+    int32_t count;
+};
+static_assert(sizeof(QItem) == 16, "QItem layout");
+
+struct DeviceTables {
+    TensorDesc *tensors = nullptr;
+    Chunk *chunks = nullptr;
+    QItem *row_items = nullptr;   // blocks with qrows == 1
+    QItem *tile_items = nullptr;  // blocks with qrows > 1 (one block per item)
+    void *base = nullptr;
+    size_t bytes = 0;
+    int device = -1;
+};
+
+// Launchers (one kernel launch over the whole group each; the norm adds a
+// small fixed-order finalisation launch).  They return a cudaError_t value.
+int launch_pack(const dbuf_plan_t *p, const void *const *src, int src_dt, void *buf, int buf_dt,
+                void *stream);
+int launch_unpack(const dbuf_plan_t *p, const void *buf, int buf_dt, void *const *dst, int dst_dt,
+                  void *stream);
+int launch_sac(const dbuf_plan_t *p, void *grad, int grad_dt, float *acc, float scale,
+               void *stream);
+int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_norms,
+                float *total_norm, int32_t *nonfinite, void *workspace, void *stream);
+int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *scales,
+                 void *stream);
+
+size_t norm_workspace_bytes(const dbuf_plan_t *p);
+
+}  // namespace dbuf
+
+struct dbuf_plan {
+    int32_t n = 0;
+    int32_t m = 0;
+    int64_t align = 1;
+    bool even = true;
+    std::vector<int32_t> units;  // m shares (all 1 when even)
+    std::vector<dbuf_tensor_spec> specs;
+
+    int64_t S = 0;
+    int64_t total = 0;
+    std::vector<int64_t> offsets;        // [n]
+    std::vector<int64_t> bounds;         // [m+1]
+    std::vector<int64_t> scale_offsets;  // [n]
+    int64_t n_scales = 0;
+
+    std::vector<dbuf::TensorDesc> tdesc;
+    std::vector<dbuf::Chunk> chunks;
+    std::vector<dbuf::QItem> row_items;
+    std::vector<dbuf::QItem> tile_items;
+
+    bool uploaded = false;
+    dbuf::DeviceTables dev;
+};

@@ -1,0 +1,201 @@
+"""Thin ctypes binding of libdbuf (include/dbuf.h): same names, argument
+marshalling only.  Every computation happens in the library (host planner and
+CUDA kernels); device memory and streams come from the caller (PyTorch in the
+tests and the benchmark) as plain integer addresses.
+
+There is no fallback: if libdbuf.so is missing this module raises on load.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "lib", "libdbuf.so")
+
+DBUF_OK = 0
+DBUF_EINVAL = -1
+DBUF_ENOMEM = -2
+DBUF_ECUDA = -3
+DBUF_ENOTUPLOADED = -4
+DBUF_ETIMEOUT = -5
+DBUF_EDEVICE = -6
+DBUF_ERANGE = -7
+
+DBUF_F32 = 0
+DBUF_BF16 = 1
+
+DBUF_QUANT_NONE = 0
+DBUF_QUANT_E4M3 = 1
+DBUF_QUANT_INT8 = 2
+
+DBUF_OP_PACK = 0
+DBUF_OP_UNPACK = 1
+DBUF_OP_SCALE_ACCUM_ZERO = 2
+DBUF_OP_NORM_NONFINITE = 3
+DBUF_OP_BLOCK_QUANT = 4
+
+_QUANT = {None: DBUF_QUANT_NONE, "none": DBUF_QUANT_NONE, "e4m3": DBUF_QUANT_E4M3,
+          "int8": DBUF_QUANT_INT8}
+
+# Every symbol include/dbuf.h declares.
+EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
+           "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
+           "dbuf_norm_nonfinite", "dbuf_block_quant", "dbuf_strerror", "dbuf_last_cuda_error")
+
+
+class DbufError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        msg = f"{where}: {code} ({_lib_handle().dbuf_strerror(code).decode()})"
+        if code == DBUF_ECUDA:
+            msg += f", cudaError {_lib_handle().dbuf_last_cuda_error()}"
+        super().__init__(msg)
+
+
+class dbuf_tensor_spec(ctypes.Structure):
+    _fields_ = [("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("gran_rows", ctypes.c_int64), ("qblock_rows", ctypes.c_int32),
+                ("qblock_cols", ctypes.c_int32), ("quant", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_lib = None
+
+
+def _lib_handle():
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"libdbuf.so is not built ({LIB_PATH}); build it with "
+                "`python -c 'import __graft_entry__ as g; g.build()'`")
+        try:
+            import torch  # noqa: F401  (loads the shared CUDA runtime first)
+        except ImportError:
+            pass
+        L = ctypes.CDLL(LIB_PATH)
+        P, i32, i64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+        L.dbuf_plan.argtypes = [P, i32, i32, P, i64, ctypes.POINTER(ctypes.c_void_p)]
+        L.dbuf_plan.restype = ctypes.c_int
+        L.dbuf_plan_query.argtypes = [P, P, P, P, P, P, P]
+        L.dbuf_plan_query.restype = ctypes.c_int
+        L.dbuf_plan_upload.argtypes = [P, P]
+        L.dbuf_plan_upload.restype = ctypes.c_int
+        L.dbuf_plan_free.argtypes = [P]
+        L.dbuf_plan_free.restype = None
+        L.dbuf_pack_cast.argtypes = [P, P, i32, P, i32, P]
+        L.dbuf_pack_cast.restype = ctypes.c_int
+        L.dbuf_unpack.argtypes = [P, P, i32, P, i32, P]
+        L.dbuf_unpack.restype = ctypes.c_int
+        L.dbuf_scale_accum_zero.argtypes = [P, P, i32, P, ctypes.c_float, P]
+        L.dbuf_scale_accum_zero.restype = ctypes.c_int
+        L.dbuf_workspace_bytes.argtypes = [P, i32]
+        L.dbuf_workspace_bytes.restype = ctypes.c_size_t
+        L.dbuf_norm_nonfinite.argtypes = [P, P, i32, P, P, P, P, ctypes.c_size_t, P]
+        L.dbuf_norm_nonfinite.restype = ctypes.c_int
+        L.dbuf_block_quant.argtypes = [P, P, P, P, P]
+        L.dbuf_block_quant.restype = ctypes.c_int
+        L.dbuf_strerror.argtypes = [ctypes.c_int]
+        L.dbuf_strerror.restype = ctypes.c_char_p
+        L.dbuf_last_cuda_error.argtypes = []
+        L.dbuf_last_cuda_error.restype = ctypes.c_int
+        _lib = L
+    return _lib
+
+
+def library():
+    """The loaded ctypes library (raises if it is not built)."""
+    return _lib_handle()
+
+
+def _check(rc: int, where: str) -> None:
+    if rc != DBUF_OK:
+        raise DbufError(rc, where)
+
+
+def _spec_array(specs) -> ctypes.Array:
+    arr = (dbuf_tensor_spec * max(len(specs), 1))()
+    for i, s in enumerate(specs):
+        if isinstance(s, (tuple, list)):
+            rows, cols, gran = s[0], s[1], s[2]
+            qb = s[3] if len(s) > 3 else (0, 0)
+            q = s[4] if len(s) > 4 else None
+        else:
+            rows, cols, gran = s.rows, s.cols, s.gran_rows
+            qb, q = getattr(s, "qblock", (0, 0)), getattr(s, "quant", None)
+        arr[i] = dbuf_tensor_spec(rows, cols, gran, qb[0], qb[1], _QUANT.get(q, q), 0)
+    return arr
+
+
+def dbuf_plan(specs: Sequence, m: int, local_units: Optional[Sequence[int]] = None,
+              align_elems: int = 16) -> int:
+    """Plan a tensor group; returns the opaque plan handle (an int)."""
+    arr = _spec_array(specs)
+    units = (ctypes.c_int32 * m)(*local_units) if local_units is not None else None
+    out = ctypes.c_void_p()
+    _check(_lib_handle().dbuf_plan(arr, len(specs), m, units, align_elems, ctypes.byref(out)),
+           "dbuf_plan")
+    return out.value
+
+
+def dbuf_plan_query(plan: int, n: int, m: int) -> dict:
+    S, total, ns = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+    off = (ctypes.c_int64 * max(n, 1))()
+    bounds = (ctypes.c_int64 * (m + 1))()
+    soff = (ctypes.c_int64 * max(n, 1))()
+    _check(_lib_handle().dbuf_plan_query(plan, ctypes.byref(S), ctypes.byref(total), off, bounds,
+                                         soff, ctypes.byref(ns)), "dbuf_plan_query")
+    return {"S": S.value, "total": total.value, "offsets": list(off)[:n],
+            "shard_bounds": list(bounds), "scale_offsets": list(soff)[:n], "n_scales": ns.value}
+
+
+def dbuf_plan_upload(plan: int, stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_plan_upload(plan, stream), "dbuf_plan_upload")
+
+
+def dbuf_plan_free(plan: int) -> None:
+    _lib_handle().dbuf_plan_free(plan)
+
+
+def dbuf_pack_cast(plan: int, src_ptrs: int, src_dtype: int, buf: int, buf_dtype: int,
+                   stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_pack_cast(plan, src_ptrs, src_dtype, buf, buf_dtype, stream),
+           "dbuf_pack_cast")
+
+
+def dbuf_unpack(plan: int, buf: int, buf_dtype: int, dst_ptrs: int, dst_dtype: int,
+                stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_unpack(plan, buf, buf_dtype, dst_ptrs, dst_dtype, stream),
+           "dbuf_unpack")
+
+
+def dbuf_scale_accum_zero(plan: int, grad: int, grad_dtype: int, acc: int, scale: float,
+                          stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_scale_accum_zero(plan, grad, grad_dtype, acc, scale, stream),
+           "dbuf_scale_accum_zero")
+
+
+def dbuf_workspace_bytes(plan: int, op: int) -> int:
+    return int(_lib_handle().dbuf_workspace_bytes(plan, op))
+
+
+def dbuf_norm_nonfinite(plan: int, buf: int, dtype: int, tensor_norms: int, total_norm: int,
+                        nonfinite: int, workspace: int, workspace_bytes: int,
+                        stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_norm_nonfinite(plan, buf, dtype, tensor_norms, total_norm,
+                                             nonfinite, workspace, workspace_bytes, stream),
+           "dbuf_norm_nonfinite")
+
+
+def dbuf_block_quant(plan: int, buf: int, codes: int, scales: int, stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_block_quant(plan, buf, codes, scales, stream), "dbuf_block_quant")
+
+
+def dbuf_strerror(code: int) -> str:
+    return _lib_handle().dbuf_strerror(code).decode()
+
+
+def dbuf_last_cuda_error() -> int:
+    return int(_lib_handle().dbuf_last_cuda_error())

@@ -1,0 +1,169 @@
+"""DBuffer: a planned flat buffer for one tensor group, on top of the C ABI.
+
+PyTorch provides device memory and streams only; every step of the group
+operators runs in libdbuf's kernels through the binding in ``dbuf.py``.  This
+class keeps a plan handle and the device-side pointer tables of the user
+tensors, and exposes zero-copy views of each tensor inside a buffer
+("veScale-FSDP: Flexible and High-Performance FSDP at Scale", §5 DBuffer:
+zero-copy access through a persistent address mapping).
+"""
+from __future__ import annotations
+
+from typing import Dict, List, Optional, Sequence, Tuple
+
+import torch
+
+from . import dbuf as _c
+
+_DT = {torch.float32: _c.DBUF_F32, torch.bfloat16: _c.DBUF_BF16}
+
+
+def dtype_code(t: torch.dtype) -> int:
+    try:
+        return _DT[t]
+    except KeyError:
+        raise TypeError(f"DBuffer buffers are float32 or bfloat16, not {t}") from None
+
+
+class DBuffer:
+    """One planned tensor group: layout, descriptor tables on the device, and
+    the group operators over buffers of that layout."""
+
+    def __init__(self, specs: Sequence, m: int, local_units: Optional[Sequence[int]] = None,
+                 align_elems: int = 16, device: Optional[torch.device] = None):
+        self.specs = list(specs)
+        self.n = len(self.specs)
+        self.m = m
+        self.local_units = list(local_units) if local_units is not None else None
+        self.handle = _c.dbuf_plan(self.specs, m, local_units, align_elems)
+        q = _c.dbuf_plan_query(self.handle, self.n, m)
+        self.S: int = q["S"]
+        self.total: int = q["total"]
+        self.offsets: List[int] = q["offsets"]
+        self.shard_bounds: List[int] = q["shard_bounds"]
+        self.scale_offsets: List[int] = q["scale_offsets"]
+        self.n_scales: int = q["n_scales"]
+        self.numel = [int(s.rows) * int(s.cols) if not isinstance(s, (tuple, list))
+                      else int(s[0]) * int(s[1]) for s in self.specs]
+        self.device = torch.device(device if device is not None else "cuda")
+        self._ptr_tables: Dict[Tuple[int, ...], torch.Tensor] = {}
+        self._workspace: Optional[torch.Tensor] = None
+        self.uploaded = False
+
+    # -- lifetime ------------------------------------------------------------
+    def upload(self, stream: Optional[torch.cuda.Stream] = None) -> "DBuffer":
+        with torch.cuda.device(self.device):
+            st = stream if stream is not None else torch.cuda.current_stream()
+            _c.dbuf_plan_upload(self.handle, st.cuda_stream)
+        self.uploaded = True
+        return self
+
+    def close(self) -> None:
+        if self.handle:
+            _c.dbuf_plan_free(self.handle)
+            self.handle = 0
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- memory helpers (allocation only) -------------------------------------
+    def new_buffer(self, dtype: torch.dtype, zero: bool = True) -> torch.Tensor:
+        """A flat buffer of `total` elements; padding starts (and stays) zero."""
+        f = torch.zeros if zero else torch.empty
+        return f(self.total, dtype=dtype, device=self.device)
+
+    def view(self, buf: torch.Tensor, t: int) -> torch.Tensor:
+        """Zero-copy view of tensor t inside `buf`."""
+        s = self.specs[t]
+        rows, cols = (s[0], s[1]) if isinstance(s, (tuple, list)) else (s.rows, s.cols)
+        o = self.offsets[t]
+        return buf[o:o + rows * cols].view(rows, cols)
+
+    def ptr_table(self, tensors: Sequence[torch.Tensor]) -> torch.Tensor:
+        """Device array of the tensors' data pointers (cached per pointer tuple)."""
+        if len(tensors) != self.n:
+            raise ValueError(f"expected {self.n} tensors, got {len(tensors)}")
+        for t, x in zip(range(self.n), tensors):
+            if not x.is_contiguous() or x.numel() != self.numel[t]:
+                raise ValueError(f"tensor {t} must be contiguous with {self.numel[t]} elements")
+            if x.device != self.device:
+                raise ValueError(f"tensor {t} is on {x.device}, expected {self.device}")
+        key = tuple(int(x.data_ptr()) for x in tensors)
+        tab = self._ptr_tables.get(key)
+        if tab is None:
+            tab = torch.tensor(list(key) if key else [0], dtype=torch.int64, device=self.device)
+            self._ptr_tables[key] = tab
+        return tab
+
+    def workspace(self) -> torch.Tensor:
+        nbytes = _c.dbuf_workspace_bytes(self.handle, _c.DBUF_OP_NORM_NONFINITE)
+        if self._workspace is None or self._workspace.numel() < nbytes:
+            self._workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+        return self._workspace
+
+    # -- group operators ---------------------------------------------------------
+    @staticmethod
+    def _stream(stream):
+        return (stream if stream is not None else torch.cuda.current_stream()).cuda_stream
+
+    def _check_buf(self, buf: torch.Tensor):
+        if buf.numel() < self.total or not buf.is_contiguous() or buf.device != self.device:
+            raise ValueError("buffer must be a contiguous device tensor of `total` elements")
+
+    def pack_cast(self, srcs: Sequence[torch.Tensor], buf: torch.Tensor, stream=None) -> None:
+        self._check_buf(buf)
+        sdt = dtype_code(srcs[0].dtype) if srcs else _c.DBUF_F32
+        if any(dtype_code(x.dtype) != sdt for x in srcs):
+            raise TypeError("all source tensors must share one dtype")
+        tab = self.ptr_table(srcs)
+        _c.dbuf_pack_cast(self.handle, tab.data_ptr(), sdt, buf.data_ptr(), dtype_code(buf.dtype),
+                          self._stream(stream))
+
+    def unpack(self, buf: torch.Tensor, dsts: Sequence[torch.Tensor], stream=None) -> None:
+        self._check_buf(buf)
+        ddt = dtype_code(dsts[0].dtype) if dsts else _c.DBUF_F32
+        if any(dtype_code(x.dtype) != ddt for x in dsts):
+            raise TypeError("all destination tensors must share one dtype")
+        tab = self.ptr_table(dsts)
+        _c.dbuf_unpack(self.handle, buf.data_ptr(), dtype_code(buf.dtype), tab.data_ptr(), ddt,
+                       self._stream(stream))
+
+    def scale_accum_zero(self, grad: torch.Tensor, acc: torch.Tensor, scale: float,
+                         stream=None) -> None:
+        self._check_buf(grad)
+        self._check_buf(acc)
+        if acc.dtype != torch.float32:
+            raise TypeError("the accumulator is float32")
+        _c.dbuf_scale_accum_zero(self.handle, grad.data_ptr(), dtype_code(grad.dtype),
+                                 acc.data_ptr(), float(scale), self._stream(stream))
+
+    def norm_nonfinite(self, buf: torch.Tensor, out: Optional[Tuple] = None, stream=None):
+        """Returns device tensors (tensor_norms[n] f32, total_norm[1] f32, nonfinite[1] i32)."""
+        self._check_buf(buf)
+        if out is None:
+            out = (torch.empty(max(self.n, 1), dtype=torch.float32, device=self.device),
+                   torch.empty(1, dtype=torch.float32, device=self.device),
+                   torch.empty(1, dtype=torch.int32, device=self.device))
+        norms, total, flag = out
+        ws = self.workspace()
+        _c.dbuf_norm_nonfinite(self.handle, buf.data_ptr(), dtype_code(buf.dtype),
+                               norms.data_ptr(), total.data_ptr(), flag.data_ptr(),
+                               ws.data_ptr(), ws.numel(), self._stream(stream))
+        return norms[:self.n], total, flag
+
+    def block_quant(self, buf: torch.Tensor, codes: Optional[torch.Tensor] = None,
+                    scales: Optional[torch.Tensor] = None, stream=None):
+        """Returns (codes uint8[total], scales f32[n_scales])."""
+        self._check_buf(buf)
+        if buf.dtype != torch.float32:
+            raise TypeError("block quantisation reads a float32 buffer")
+        if codes is None:
+            codes = torch.zeros(self.total, dtype=torch.uint8, device=self.device)
+        if scales is None:
+            scales = torch.empty(max(self.n_scales, 1), dtype=torch.float32, device=self.device)
+        _c.dbuf_block_quant(self.handle, buf.data_ptr(), codes.data_ptr(), scales.data_ptr(),
+                            self._stream(stream))
+        return codes, scales[:self.n_scales]

@@ -1,0 +1,254 @@
+/*
+ * dbuf.h -- C ABI of libdbuf: the DBuffer group-operator path on one GPU.
+ *
+ * A DBuffer is one flat buffer that holds a group of tensors, laid out by the
+ * planner so that the buffer splits into m shard slices of S elements (or of
+ * u_k * U elements with uneven local_units) without cutting any block of any
+ * tensor, with padding only between tensors.  Every group operator runs over the
+ * whole tensor group in one kernel launch driven by a device-side descriptor
+ * table, touching the tensor ranges only (padding is never read or written).
+ *
+ * Passages these calls implement (page title, section):
+ *  - "veScale-FSDP: Flexible and High-Performance FSDP at Scale": §4 RaggedShard
+ *    format (element/row/block granularity, any per-device distribution; block
+ *    and shard boundaries coincide); §5 Planning algorithm (formulation: minimise
+ *    the per-shard size S, unsharded blocks, contiguous tensor memory, balanced
+ *    load; default tensor order; 3-case analysis); §5 DBuffer (group-level
+ *    operators fusing add/scale/zero/copy across the tensor group; zero-copy
+ *    access through a persistent address mapping); Figure 2 (copy-in before
+ *    ReduceScatter / copy-out after AllGather); §6.3 (block-wise quantisation of
+ *    the local shard without communication).
+ *  - "PyTorch FSDP: Experiences on Scaling Fully Sharded Data Parallel":
+ *    FlatParameter (flatten, pad, shard evenly); native mixed precision (one
+ *    cast per flat parameter); gradient accumulation without communication;
+ *    sharded gradient scaler; known limitations (per-parameter norms).
+ *  - "veScale 深度技术分析": RaggedShard Placement (dims, local_units, flattened
+ *    storage, reconstruct_tensor_from_flat); OpDispatcher (ragged norm handler,
+ *    found_inf / non-finite check handler).
+ *
+ * Conventions for every call:
+ *  - Ownership: the caller owns every device buffer and every stream; the
+ *    library owns the plan and its device descriptor table.  A plan is
+ *    immutable after dbuf_plan_upload and may be shared across host threads.
+ *  - Execution: operators are asynchronous on `stream` (a cudaStream_t passed as
+ *    void*, NULL = the legacy default stream).  Argument checks are synchronous
+ *    and happen before any launch; a rejected call touches no GPU memory.
+ *  - Device: a plan is uploaded to the device current at dbuf_plan_upload and
+ *    its operators must be called with that device current (else DBUF_EDEVICE).
+ *  - Pointers: device pointers should be 16-byte aligned; a chunk whose source
+ *    or destination is not takes a slower scalar path with identical results.
+ *  - Errors: 0 = DBUF_OK, negative = error code (see below).  No exception or
+ *    abort crosses the ABI.  A failed kernel launch returns DBUF_ECUDA and the
+ *    cudaError_t is kept for dbuf_last_cuda_error() (per host thread).
+ */
+#ifndef FSDP_INFRA_GB300_DBUF_H
+#define FSDP_INFRA_GB300_DBUF_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Return codes. */
+#define DBUF_OK 0
+#define DBUF_EINVAL (-1)       /* bad argument: null pointer, bad size, bad dtype */
+#define DBUF_ENOMEM (-2)       /* host or device allocation failed */
+#define DBUF_ECUDA (-3)        /* a CUDA call or launch failed */
+#define DBUF_ENOTUPLOADED (-4) /* operator called on a plan not yet uploaded */
+#define DBUF_ETIMEOUT (-5)     /* reserved: a bounded device-side wait gave up */
+#define DBUF_EDEVICE (-6)      /* current device differs from the plan's device */
+#define DBUF_ERANGE (-7)       /* a size exceeds what the call supports */
+
+/* Element types of buffers and user tensors. */
+#define DBUF_F32 0
+#define DBUF_BF16 1
+
+/* Quantisation code formats. */
+#define DBUF_QUANT_NONE 0
+#define DBUF_QUANT_E4M3 1 /* OCP FP8 E4M3: bias 7, max 448, no infinity */
+#define DBUF_QUANT_INT8 2 /* symmetric int8 in [-127, 127] */
+
+/* Operator ids for dbuf_workspace_bytes. */
+#define DBUF_OP_PACK 0
+#define DBUF_OP_UNPACK 1
+#define DBUF_OP_SCALE_ACCUM_ZERO 2
+#define DBUF_OP_NORM_NONFINITE 3
+#define DBUF_OP_BLOCK_QUANT 4
+
+/*
+ * One tensor of the group: a row-major [rows, cols] tensor (a 1-D vector is
+ * [n, 1]).  RaggedShard acts on flattened storage with the row as the sharded
+ * prefix dimension, so the sharding unit is gran_rows whole rows:
+ * g_t = gran_rows * cols elements.  gran_rows = 0 (or >= rows) makes the whole
+ * tensor one unit that is never cut; gran_rows = 1 is row-wise RaggedShard; a
+ * vector with gran_rows = 1 is element-granular.
+ * quant / qblock_rows x qblock_cols: the block-wise quantisation of this tensor
+ * (0 extents = the whole dimension; edge blocks are clipped).  A quantised
+ * tensor needs shard cuts that never split a quantisation block: gran_rows must
+ * be 0, >= rows, or a multiple of qblock_rows.
+ * 40 bytes, no implicit padding.
+ */
+typedef struct dbuf_tensor_spec {
+    int64_t rows;
+    int64_t cols;
+    int64_t gran_rows;
+    int32_t qblock_rows;
+    int32_t qblock_cols;
+    int32_t quant;
+    int32_t reserved; /* must be 0 */
+} dbuf_tensor_spec;
+
+/* Opaque plan: layout, per-tensor offsets, shard bounds and the descriptor
+ * tables of the group operators. */
+typedef struct dbuf_plan dbuf_plan_t;
+
+/*
+ * dbuf_plan -- host only, no CUDA call.  Plans the layout of n tensors (in the
+ * given order, which is kept: the pages adopt the default order) into one flat
+ * buffer of m shard slices.  [veScale-FSDP §5 Planning algorithm, formulation.]
+ * It returns the minimum per-shard size S, a multiple of align_elems, such that
+ * offsets l_t exist with: (i) tensors in order without overlap, padding only
+ * between tensors; (ii) every l_t a multiple of align_elems; (iii) a shard
+ * boundary strictly inside tensor t lies a multiple of g_t from l_t (no block is
+ * split); (iv) the last tensor ends inside the buffer.  The offsets are the
+ * greedy-leftmost ones at that S (each l_t the smallest value allowed given
+ * l_{t-1}), which makes the plan unique and deterministic.
+ * local_units: NULL for even shards (shard k = [k*S, (k+1)*S)); otherwise m
+ * positive shares u_k (RaggedShard local_units): shard k holds u_k*S elements
+ * and S (the size of one unit) is minimised.
+ * specs: host array of n specs (copied).  n may be 0.  m >= 1.
+ * align_elems >= 1 (16 makes every offset 64-byte aligned for fp32).
+ * On success *out owns a new plan (free with dbuf_plan_free).
+ * Errors: DBUF_EINVAL (bad spec or argument), DBUF_ERANGE (sizes overflow),
+ * DBUF_ENOMEM.
+ */
+int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
+              const int32_t *local_units, int64_t align_elems, dbuf_plan_t **out);
+
+/*
+ * dbuf_plan_query -- host only.  Copies the plan's results into host arrays;
+ * any output pointer may be NULL.
+ *   S            per-shard size (the unit size U when local_units were given)
+ *   total        buffer length in elements: S * sum(u_k) (= m*S for even shards)
+ *   offsets      [n]   l_t, element offset of tensor t in the buffer
+ *   shard_bounds [m+1] B_k, element offset where shard k starts (B_m = total)
+ *   scale_offsets[n]   index of tensor t's first block scale (tensors without
+ *                      quantisation take no scales)
+ *   n_scales     number of block scales of the whole group
+ * Errors: DBUF_EINVAL if plan is NULL.
+ */
+int dbuf_plan_query(const dbuf_plan_t *plan, int64_t *S, int64_t *total, int64_t *offsets,
+                    int64_t *shard_bounds, int64_t *scale_offsets, int64_t *n_scales);
+
+/*
+ * dbuf_plan_upload -- copies the plan's descriptor tables (tensor table, chunk
+ * table, quantisation work lists) to the current device: the persistent
+ * address mapping of [veScale-FSDP §5 DBuffer, zero-copy access].  Allocates
+ * device memory owned by the plan and waits for the copies on `stream`.
+ * Uploading twice on the same device is a no-op.
+ * Errors: DBUF_EINVAL, DBUF_ENOMEM, DBUF_ECUDA, DBUF_EDEVICE (already uploaded
+ * to another device).
+ */
+int dbuf_plan_upload(dbuf_plan_t *plan, void *stream);
+
+/* dbuf_plan_free -- frees the plan and its device tables (cudaFree, which
+ * waits for the device); no operator may still be running on it.  NULL is a
+ * no-op. */
+void dbuf_plan_free(dbuf_plan_t *plan);
+
+/*
+ * dbuf_pack_cast -- copy-in with the mixed-precision cast fused:
+ * buf[l_t + i] = cast(src_t[i]) for every tensor t and i < n_t.
+ * [veScale-FSDP §5 DBuffer group-level operators; Figure 2 copy-in; PyTorch
+ * FSDP native mixed precision.]
+ * src: DEVICE array of n device pointers (8 bytes each), one contiguous tensor
+ * of n_t elements of src_dtype per entry; owned by the caller, read by the
+ * kernel, so it must stay valid until the operation completes.
+ * buf: device buffer of `total` elements of buf_dtype.  Padding is not written.
+ * Casts: f32->f32 and bf16->bf16 copy bits; f32->bf16 rounds to nearest even
+ * (NaN stays NaN); bf16->f32 is exact.
+ * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_pack_cast(const dbuf_plan_t *plan, const void *const *src, int32_t src_dtype,
+                   void *buf, int32_t buf_dtype, void *stream);
+
+/*
+ * dbuf_unpack -- copy-out / reconstruct each tensor from the flat buffer:
+ * dst_t[i] = cast(buf[l_t + i]).  [veScale-FSDP Figure 2 copy-out; veScale
+ * RaggedShard Placement, reconstruct_tensor_from_flat.]
+ * dst: DEVICE array of n device pointers (caller-owned), dst_dtype elements.
+ * Same casts and errors as dbuf_pack_cast.
+ */
+int dbuf_unpack(const dbuf_plan_t *plan, const void *buf, int32_t buf_dtype,
+                void *const *dst, int32_t dst_dtype, void *stream);
+
+/*
+ * dbuf_scale_accum_zero -- gradient scale, accumulate and zero, fused across
+ * the group: over every tensor range, acc[j] = acc[j] + grad[j]*scale with the
+ * product and the sum each rounded to fp32 (no fused multiply-add), then
+ * grad[j] = +0.  [veScale-FSDP §5 DBuffer group-level operators (add, scale,
+ * zero); PyTorch FSDP gradient accumulation without communication.]
+ * grad: device buffer of grad_dtype (DBUF_F32 or DBUF_BF16); acc: device fp32
+ * buffer; both `total` elements with the plan's layout.  Padding untouched.
+ * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_scale_accum_zero(const dbuf_plan_t *plan, void *grad, int32_t grad_dtype, float *acc,
+                          float scale, void *stream);
+
+/*
+ * dbuf_workspace_bytes -- device scratch needed by an operator for this plan
+ * (0 when it needs none).  Only DBUF_OP_NORM_NONFINITE needs scratch.
+ */
+size_t dbuf_workspace_bytes(const dbuf_plan_t *plan, int32_t op);
+
+/*
+ * dbuf_norm_nonfinite -- per-tensor L2 norms over the ragged shards, the global
+ * L2 norm, and a flag for any non-finite value (inf or NaN) in any tensor range.
+ * [veScale OpDispatcher: ragged norm handler and non-finite check handler;
+ * PyTorch FSDP sharded gradient scaler and known limitations.]
+ * Sums of squares are accumulated per chunk in fp32 and combined in fp64 in a
+ * fixed order (deterministic, run to run); norms are returned in fp32.
+ * buf: device buffer of dtype (DBUF_F32 or DBUF_BF16).  Outputs are device
+ * pointers: tensor_norms [n] floats, total_norm 1 float, nonfinite 1 int32
+ * (0 or 1).  When the flag is 1 the norms are not meaningful.
+ * workspace: caller-owned device scratch of at least
+ * dbuf_workspace_bytes(plan, DBUF_OP_NORM_NONFINITE) bytes, 256-byte aligned;
+ * it must not be shared by operations that may overlap on the GPU.
+ * Errors: DBUF_EINVAL (also for a too-small workspace), DBUF_ENOTUPLOADED,
+ * DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_norm_nonfinite(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
+                        float *tensor_norms, float *total_norm, int32_t *nonfinite,
+                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * dbuf_block_quant -- block-wise absmax quantisation of an fp32 buffer, blocks
+ * never crossing a shard boundary, so each shard quantises without
+ * communication.  [veScale-FSDP §4 Block-wise RaggedShard; §6.3 8-bit Adam.]
+ * Per block of a quantised tensor: amax = max |x|; scale = amax / qmax (one fp32
+ * division; qmax = 448 for E4M3, 127 for INT8), replaced by 1.0 if not positive;
+ * code = enc(x / scale) with an fp32 division: E4M3 rounds to nearest even and
+ * saturates to +-448; INT8 rounds half to even and clamps to [-127, 127].
+ * buf: device fp32 buffer (`total` elements).  codes: device uint8 buffer of
+ * `total` bytes, same layout; bytes outside quantised tensors are untouched.
+ * scales: device fp32 array of n_scales entries, tensor by tensor in row-major
+ * block order starting at scale_offsets[t].  Inputs with inf/NaN give
+ * unspecified codes.
+ * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, float *scales,
+                     void *stream);
+
+/* dbuf_strerror -- static description of a return code. */
+const char *dbuf_strerror(int code);
+
+/* dbuf_last_cuda_error -- cudaError_t of the last DBUF_ECUDA on this thread. */
+int dbuf_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FSDP_INFRA_GB300_DBUF_H */
