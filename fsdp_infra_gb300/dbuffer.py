@@ -45,7 +45,10 @@ class DBuffer:
         self.n_scales: int = q["n_scales"]
         self.numel = [int(s.rows) * int(s.cols) if not isinstance(s, (tuple, list))
                       else int(s[0]) * int(s[1]) for s in self.specs]
-        self.device = torch.device(device if device is not None else "cuda")
+        dev = torch.device(device if device is not None else "cuda")
+        if dev.type == "cuda" and dev.index is None and torch.cuda.is_available():
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
         self._ptr_tables: Dict[Tuple[int, ...], torch.Tensor] = {}
         self._workspace: Optional[torch.Tensor] = None
         self.uploaded = False

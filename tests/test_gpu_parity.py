@@ -264,7 +264,7 @@ def test_fp8_and_int8_encoding_sweep(lib, oracle_lib):
     x = np.zeros(rows * cols, np.float32)
     x[:vals.size] = vals
     x = x.reshape(rows, cols)
-    halves = np.arange(-127.5, 128.0, 0.5, dtype=np.float32)       # exact ties included
+    halves = np.arange(-126.5, 127.0, 0.5, dtype=np.float32)       # exact ties included
     rnd = np.random.default_rng(8).uniform(-127, 127, rows * cols - halves.size).astype(np.float32)
     xi = np.concatenate([halves, rnd]).reshape(rows, cols)
     for q, qmax, qb in [("e4m3", 448.0, (rows, cols)), ("int8", 127.0, (1, cols))]:
