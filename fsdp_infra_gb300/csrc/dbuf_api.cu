@@ -36,6 +36,8 @@ int finish(int e) { return e == cudaSuccess ? DBUF_OK : cuda_fail(cudaError_t(e)
 
 extern "C" int dbuf_last_cuda_error(void) { return g_last_cuda_error; }
 
+void dbuf::record_cuda_error(int e) { g_last_cuda_error = e; }
+
 extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     if (!p) return DBUF_EINVAL;
     int dev = -1;

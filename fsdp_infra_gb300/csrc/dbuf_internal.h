@@ -75,6 +75,9 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p);
 
+// Keeps a cudaError_t for dbuf_last_cuda_error() (per host thread).
+void record_cuda_error(int e);
+
 }  // namespace dbuf
 
 struct dbuf_plan {

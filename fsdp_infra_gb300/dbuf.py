@@ -42,7 +42,11 @@ _QUANT = {None: DBUF_QUANT_NONE, "none": DBUF_QUANT_NONE, "e4m3": DBUF_QUANT_E4M
 # Every symbol include/dbuf.h declares.
 EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
-           "dbuf_norm_nonfinite", "dbuf_block_quant", "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
+           "dbuf_strerror", "dbuf_last_cuda_error")
+
+# Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
+DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
 
 
 class DbufError(RuntimeError):
@@ -95,6 +99,8 @@ def _lib_handle():
         L.dbuf_workspace_bytes.restype = ctypes.c_size_t
         L.dbuf_norm_nonfinite.argtypes = [P, P, i32, P, P, P, P, ctypes.c_size_t, P]
         L.dbuf_norm_nonfinite.restype = ctypes.c_int
+        L.dbuf_norm_nonfinite_noalloc.argtypes = [P, P, i32, P, P, P, P]
+        L.dbuf_norm_nonfinite_noalloc.restype = ctypes.c_int
         L.dbuf_block_quant.argtypes = [P, P, P, P, P]
         L.dbuf_block_quant.restype = ctypes.c_int
         L.dbuf_strerror.argtypes = [ctypes.c_int]
@@ -187,6 +193,15 @@ def dbuf_norm_nonfinite(plan: int, buf: int, dtype: int, tensor_norms: int, tota
     _check(_lib_handle().dbuf_norm_nonfinite(plan, buf, dtype, tensor_norms, total_norm,
                                              nonfinite, workspace, workspace_bytes, stream),
            "dbuf_norm_nonfinite")
+
+
+def dbuf_norm_nonfinite_noalloc(plan: int, buf: int, dtype: int, tensor_norms: int,
+                                total_norm: int, nonfinite: int, stream: int = 0) -> None:
+    """dbuf_norm_nonfinite without a workspace, for callers that cannot allocate
+    device memory: the library's static scratch is used instead (see dbuf.h)."""
+    _check(_lib_handle().dbuf_norm_nonfinite_noalloc(plan, buf, dtype, tensor_norms, total_norm,
+                                                     nonfinite, stream),
+           "dbuf_norm_nonfinite_noalloc")
 
 
 def dbuf_block_quant(plan: int, buf: int, codes: int, scales: int, stream: int = 0) -> None:

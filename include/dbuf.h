@@ -241,6 +241,32 @@ int dbuf_norm_nonfinite(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
 int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, float *scales,
                      void *stream);
 
+/*
+ * dbuf_norm_nonfinite_noalloc -- the same per-tensor norms, global norm and
+ * non-finite flag as dbuf_norm_nonfinite, for callers that cannot allocate
+ * device memory and so cannot pass a workspace: for example a host program
+ * that links only this C ABI while its framework holds the device memory in its
+ * own pool (a cudaMalloc would fail or fragment that pool), or an out-of-memory
+ * recovery path that must still check gradients for inf/NaN before deciding
+ * to skip a step.  The pages have no counterpart to this entry point.
+ * Scratch: a static device array of DBUF_NOALLOC_SCRATCH_BYTES inside the
+ * library, held by every device that loads it until the process exits.  A plan
+ * whose norm needs more (dbuf_workspace_bytes(plan, DBUF_OP_NORM_NONFINITE) >
+ * DBUF_NOALLOC_SCRATCH_BYTES, about 87,000 chunks or 1.4e9 elements) is
+ * rejected with DBUF_ERANGE before anything is launched.  The first call on a
+ * device looks up the array's device address (once per device, with that
+ * device current); make that first call before any stream capture.  All calls
+ * share the one array: calls that may overlap on the GPU (other streams, other
+ * host threads) race on it, so the caller must serialise them.  Nothing in the
+ * scratch needs to start at zero; each call writes all it reads.  The call
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * Arguments, outputs and other errors as for dbuf_norm_nonfinite.
+ */
+#define DBUF_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
+int dbuf_norm_nonfinite_noalloc(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
+                                float *tensor_norms, float *total_norm, int32_t *nonfinite,
+                                void *stream);
+
 /* dbuf_strerror -- static description of a return code. */
 const char *dbuf_strerror(int code);
 
