@@ -122,7 +122,14 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # workload: every DBuffer of the 7B-shaped stack
 # ---------------------------------------------------------------------------
-OP_BYTES = {"pack_cast": 6, "unpack": 4, "scale_accum_zero": 16, "norm_nonfinite": 4}
+def op_bytes_per_elem(grad_dtype):
+    """Algorithmic bytes per element of each operator in the step (padding is
+    never touched): pack_cast reads fp32 and writes bf16; unpack reads and writes
+    bf16; scale_accum_zero reads the gradient and the fp32 accumulator, writes
+    both; norm_nonfinite reads the fp32 accumulator.  block_quant (5 B/elem plus
+    4 B per block scale) is counted per quantised element separately."""
+    g = 2 if grad_dtype == torch.bfloat16 else 4
+    return {"pack_cast": 6, "unpack": 4, "scale_accum_zero": 2 * g + 8, "norm_nonfinite": 4}
 
 
 class Stack:
@@ -166,7 +173,8 @@ class Stack:
                                    "out": out})
         self.elements = sum(g.numel * (g.repeat if layers is None else min(g.repeat, layers))
                             for g in w.groups)
-        self.op_bytes = {k: v * self.elements for k, v in OP_BYTES.items()}
+        self.per_elem = op_bytes_per_elem(w.grad_dtype)
+        self.op_bytes = {k: v * self.elements for k, v in self.per_elem.items()}
         qe, ns = 0, 0
         for d in self.dbufs:
             k = d["kind"]
@@ -174,7 +182,14 @@ class Stack:
             ns += k["db"].n_scales
         self.op_bytes["block_quant"] = 5 * qe + 4 * ns
         self.bytes_per_step = sum(self.op_bytes.values())
-        self.launches_per_step = 6 * len(self.dbufs)  # pack, unpack, sac, norm x2, quant
+        # pack, unpack, scale_accum_zero, norm (per-chunk partials + finalise) and one
+        # quantisation launch per kind of block present (tiles, row blocks).
+        self.launches_per_step = 0
+        for d in self.dbufs:
+            spec = d["kind"]["spec"]
+            qkinds = {("tile" if (s.qblock[0] or s.rows) > 1 else "row")
+                      for s in spec.tensors if s.quant and s.numel}
+            self.launches_per_step += 5 + len(qkinds)
 
     def step(self, timers=None):
         w = self.w
@@ -199,15 +214,65 @@ class Stack:
                 timers.mark("block_quant", 1)
 
 
-class OpTimers:
-    """CUDA events around every operator launch on the launching stream."""
+class RawEvent:
+    """A CUDA timing event recorded with cudaEventRecordExternal, so that inside a
+    stream capture it becomes a timestamp node of the graph (a plain record there
+    only marks a dependency).  Uses the CUDA runtime PyTorch already loaded."""
+    _rt = None
+
+    @classmethod
+    def rt(cls):
+        if cls._rt is None:
+            import ctypes
+            rt = ctypes.CDLL("libcudart.so.13")
+            rt.cudaEventCreate.argtypes = [ctypes.POINTER(ctypes.c_void_p)]
+            rt.cudaEventRecordWithFlags.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint]
+            rt.cudaEventElapsedTime.argtypes = [ctypes.POINTER(ctypes.c_float), ctypes.c_void_p,
+                                                ctypes.c_void_p]
+            rt.cudaEventDestroy.argtypes = [ctypes.c_void_p]
+            cls._rt = rt
+        return cls._rt
 
     def __init__(self):
+        import ctypes
+        self.h = ctypes.c_void_p()
+        assert self.rt().cudaEventCreate(ctypes.byref(self.h)) == 0
+
+    def record(self, stream):
+        assert self.rt().cudaEventRecordWithFlags(self.h, stream.cuda_stream, 1) == 0
+
+    def elapsed_time(self, end):
+        import ctypes
+        ms = ctypes.c_float()
+        assert self.rt().cudaEventElapsedTime(ctypes.byref(ms), self.h, end.h) == 0
+        return ms.value
+
+    def __del__(self):
+        try:
+            self.rt().cudaEventDestroy(self.h)
+        except Exception:
+            pass
+
+
+class OpTimers:
+    """CUDA events around operator launches on the launching stream (all
+    operators, or only `only`); raw external events work inside graph capture."""
+
+    def __init__(self, only=None, raw=False):
+        self.only = only
+        self.raw = raw
         self.events = {}
 
     def mark(self, op, which):
-        e = torch.cuda.Event(enable_timing=True)
-        e.record(torch.cuda.current_stream())
+        if self.only is not None and op != self.only:
+            return
+        st = torch.cuda.current_stream()
+        if self.raw:
+            e = RawEvent()
+            e.record(st)
+        else:
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(st)
         self.events.setdefault(op, [[], []])[which].append(e)
 
     def totals_ms(self):
@@ -276,7 +341,7 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1000 * total / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": _config_dict(None),
+            "config": _config_dict(None, "dense7b"),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": desc},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -285,16 +350,25 @@ def run_reference(args):
     return 0
 
 
-def _config_dict(stack):
-    d = {"workload": "7B-shaped dense stack: 32 layers d=4096 ffn=11008 (Wqkv 4096x12288, "
-                     "Wo 4096x4096, gate/up 4096x11008, down 11008x4096, 2 norms) + embedding "
-                     "32000x4096; one DBuffer per layer, m=64, 128x128 blocks, E4M3 128x128 "
-                     "block quant, s=1/64",
-         "dbuffers": 33, "m": 64,
+def _config_dict(stack, key):
+    from workloads import workload
+    w = workload(key)
+    if key == "dense7b":
+        desc = ("7B-shaped dense stack: 32 layers d=4096 ffn=11008 (Wqkv 4096x12288, "
+                "Wo 4096x4096, gate/up 4096x11008, down 11008x4096, 2 norms) + embedding "
+                "32000x4096; one DBuffer per layer, m=64, 128x128 blocks, E4M3 128x128 "
+                "block quant, s=1/64")
+    else:
+        desc = w.description
+    gdt = "bf16" if w.grad_dtype == torch.bfloat16 else "f32"
+    quant = sorted({s.quant for g in w.groups for s in g.tensors if s.quant})
+    d = {"workload": desc, "key": key,
+         "dbuffers": sum(g.repeat for g in w.groups), "m": w.m,
          "ops_per_dbuffer": ["pack_cast f32->bf16", "unpack bf16->bf16",
-                             "scale_accum_zero f32", "norm_nonfinite f32", "block_quant e4m3"],
-         "l2": "inputs larger than L2: each DBuffer's tensor ranges are 0.52-0.81 GB, "
-               "L2 is 129 MB"}
+                             f"scale_accum_zero {gdt} grad", "norm_nonfinite f32",
+                             "block_quant " + "+".join(quant) if quant else "block_quant none"],
+         "l2": "inputs larger than L2 (129 MB)" if w.total_numel * 4 > 129e6 * 2
+               else "inputs near or below L2 size: L2 not flushed (small case)"}
     if stack is not None:
         d["elements_per_step"] = stack.elements
         d["bytes_per_step"] = stack.bytes_per_step
@@ -336,7 +410,7 @@ def run_ours(args):
     device = torch.device("cuda", torch.cuda.current_device())
     from fsdp_infra_gb300 import build as _b  # noqa: F401  (library must already be built)
     from workloads import workload
-    w = workload("dense7b")
+    w = workload(args.workload)
     stack = Stack(w, device)
     torch.cuda.synchronize()
 
@@ -348,17 +422,49 @@ def run_ours(args):
     for _ in range(max(args.warmup, 0)):
         stack.step()
     torch.cuda.synchronize()
+    peak, peak_kind = _peaks()
+
+    # Per-operator breakdown: one instrumented eager step (outside the timed region).
+    probe = OpTimers()
+    stack.step(probe)
+    torch.cuda.synchronize()
+    per_op_eager = probe.totals_ms()
+    ops = {}
+    for op, durs in per_op_eager.items():
+        if stack.op_bytes.get(op, 0) == 0 or sum(durs) <= 0:
+            continue
+        ops[op] = {"ms_per_step": round(sum(durs), 4),
+                   "mean_launch_ms": round(statistics.mean(durs), 4),
+                   "gbs": round(stack.op_bytes[op] / (sum(durs) / 1e3) / 1e9, 1),
+                   "frac": round(stack.op_bytes[op] / (sum(durs) / 1e3) / 1e9 / peak, 4)}
+    dom = max((k for k in per_op_eager if stack.op_bytes.get(k, 0) > 0),
+              key=lambda k: sum(per_op_eager[k]))
+
+    # Timed region: K steps; by default captured once as a CUDA graph (all
+    # launches of the K steps, with timing events around each launch of the
+    # dominant operator) and replayed once untimed, then once timed.
+    timers = OpTimers(only=dom, raw=not args.eager)
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                stack.step(timers)
+        graph.replay()
+        torch.cuda.synchronize()
 
     clocks = ClockSampler(device)
-    timers = OpTimers()
     barrier()
     torch.cuda.synchronize()
     clocks.start()
     t_start = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_start.record()
-    for _ in range(args.steps):
-        stack.step(timers)
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(args.steps):
+            stack.step(timers)
     t_end.record()
     torch.cuda.synchronize()
     barrier()
@@ -371,28 +477,21 @@ def run_ours(args):
         elapsed_ms = float(t.item())
     ms_per_step = elapsed_ms / args.steps
     value = world * stack.bytes_per_step / (ms_per_step / 1e3) / 1e9
-
     per_op = timers.totals_ms()
-    peak, peak_kind = _peaks()
-    ops = {}
-    for op, durs in per_op.items():
-        per_launch_bytes = stack.op_bytes[op] / len(stack.dbufs)
-        mean_ms = statistics.mean(durs)
-        ops[op] = {"ms_per_step": round(sum(durs) / args.steps, 4),
-                   "mean_launch_ms": round(mean_ms, 4),
-                   "gbs": round(stack.op_bytes[op] / (sum(durs) / args.steps / 1e3) / 1e9, 1),
-                   "frac": round(stack.op_bytes[op] / (sum(durs) / args.steps / 1e3) / 1e9 / peak, 4)}
-    dom = max(per_op, key=lambda k: sum(per_op[k]))
-    # achieved for the dominant operator: bytes of one launch on one layer DBuffer
-    # (the 32 layer launches dominate) over the mean layer-launch duration.
-    layer_db = stack.dbufs[0]["kind"]["db"]
-    layer_elems = stack.w.groups[0].numel
+
+    # achieved for the dominant operator: algorithmic bytes of one launch on a
+    # DBuffer of the group that carries most of the elements (the 32 layers of
+    # the dense stack) over the mean duration of those launches in the timed run.
+    big = max(range(len(stack.w.groups)),
+              key=lambda gi: stack.w.groups[gi].numel * stack.w.groups[gi].repeat)
+    g0 = stack.w.groups[big]
+    big_db = next(d["kind"]["db"] for d in stack.dbufs if d["kind"]["gi"] == big)
     if dom == "block_quant":
-        layer_bytes = 5 * sum(s.numel for s in stack.w.groups[0].tensors if s.quant) + 4 * layer_db.n_scales
+        layer_bytes = 5 * sum(s.numel for s in g0.tensors if s.quant) + 4 * big_db.n_scales
     else:
-        layer_bytes = OP_BYTES[dom] * layer_elems
-    n_layers = stack.w.groups[0].repeat
-    layer_durs = [d for i, d in enumerate(per_op[dom]) if (i % len(stack.dbufs)) < n_layers]
+        layer_bytes = stack.per_elem[dom] * g0.numel
+    kinds = [d["kind"]["gi"] for d in stack.dbufs]
+    layer_durs = [d for i, d in enumerate(per_op[dom]) if kinds[i % len(kinds)] == big]
     mean_layer_ms = statistics.mean(layer_durs)
     achieved = layer_bytes / (mean_layer_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": round(achieved, 1), "peak": peak,
@@ -402,7 +501,7 @@ def run_ours(args):
                 "traffic": _traffic_for(dom)}
 
     # ---- end to end: host inputs (pinned) -> device, operators, results -> host
-    e2e = run_e2e(stack, args, world)
+    e2e = None if args.no_e2e else run_e2e(stack, args, world)
 
     line = None
     if rank == 0:
@@ -417,12 +516,14 @@ def run_ours(args):
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-                "config": _config_dict(stack),
+                "config": _config_dict(stack, args.workload),
                 "params_per_s": round(world * stack.elements / (ms_per_step / 1e3), 1),
                 "frac_of_peak": round(value / world / peak, 4), "peak_kind": peak_kind,
                 "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": stack.launches_per_step * args.steps,
+                "launch": "eager" if args.eager else "cuda_graph (K steps captured once, replayed)",
+                "ops_note": "per-operator times from one instrumented eager step outside the timed region",
                 "clocks": clock_info, "ops": ops}
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -506,6 +607,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--eager", action="store_true",
+                    help="launch the timed steps one by one instead of as one CUDA graph")
+    ap.add_argument("--workload", default="dense7b",
+                    choices=["dense7b", "llama_layer", "tiny", "moe", "mixed"],
+                    help="dense7b is the benchmark; the others are small or alternate "
+                         "cases (profiling captures)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)

@@ -14,8 +14,11 @@
 // device (with that device current) asks the runtime for the array's device
 // address once and caches it; later calls reuse it.  The call then runs the
 // same two kernels as dbuf_norm_nonfinite with that address as the workspace.
-// Nothing in the scratch has to start at zero: every partial sum, flag and
-// per-tensor sum a call reads was written earlier in the same call.
+// The only scratch words that must start at zero are the completion tickets:
+// the array is zero when the library is loaded, and every call returns each
+// ticket it used to zero before it finishes, so each call finds them cleared;
+// every partial sum, flag and per-tensor sum a call reads is written earlier in
+// the same call, so nothing else depends on what a previous call left behind.
 // All calls share the one array, so calls that overlap on the GPU (different
 // streams, or several host threads) race on it and must be serialised by the
 // caller.  No cudaMalloc, cudaFree or other allocating routine is called.

@@ -5,18 +5,27 @@
 // quantisation of optimizer statistics.
 //
 // Per block: amax = max |x| (fp32); scale = amax / qmax as one IEEE fp32
-// division, 1.0 when not positive; code = enc(x / scale) with an IEEE fp32
-// division per element.  E4M3 encodes with the hardware conversion (round to
+// division, 1.0 when not positive; code = enc(x / scale), x / scale rounded to
+// nearest even in fp32 (the IEEE quotient).  The quotient is formed from the
+// block's correctly rounded reciprocal y = RN(1/scale) with Markstein's
+// correction step (P. Markstein, "Computation of elementary functions on the
+// IBM RISC System/6000 processor", IBM J. Res. Dev. 34(1), 1990): q = RN(x*y)
+// is within one ulp of x/scale, the remainder r = x - scale*q is exact in one
+// fused multiply-add, and RN(q + r*y) is the correctly rounded quotient.  The
+// remainder stays exact whenever scale >= 2^-80 (all operands' grids are then
+// no finer than the fp32 subnormal spacing wherever the code can be non-zero);
+// blocks with a smaller scale use the IEEE division instructions directly.
+// The sign is copied from x so that x = -0 gives -0 like the division.  E4M3 encodes with the hardware conversion (round to
 // nearest even, saturating to +-448); INT8 rounds half to even and clamps to
 // [-127, 127].  Codes share the buffer's layout; scales are tensor by tensor in
 // row-major block order.
 //
 // Two kernels, each one launch over the whole group:
-//  - tile kernel (blocks taller than one row, e.g. 128x128): one CTA per block;
-//    warp w holds rows w, w+8, ... in registers (one float4 per lane per row, a
-//    512-byte coalesced row segment per warp instruction), so the block is read
-//    from HBM once; the amax is a shuffle + shared-memory max; codes are
-//    written as 4-byte words.
+//  - tile kernel (blocks taller than one row, e.g. 128x128): one 512-thread CTA
+//    per block; warp w holds rows w, w+16, ... in registers (one float4 per
+//    lane per row, a 512-byte coalesced row segment per warp instruction), so
+//    the block is read from HBM once; the amax is a shuffle + shared-memory
+//    max; codes are written as 4-byte words.
 //  - row kernel (1 x qc blocks, e.g. 1x128): one warp per block, 4 blocks per
 //    warp and 32 per CTA, loads for all 4 blocks in flight before reducing.
 // Shapes outside the vector fast path (odd widths, unaligned rows, blocks
@@ -27,7 +36,9 @@
 namespace dbuf {
 namespace {
 
-constexpr int kTileRowsPerWarp = 16;  // 8 warps x 16 rows = 128-row tiles
+constexpr int kTileThreads = 512;     // one CTA per tile
+constexpr int kTileWarps = kTileThreads / 32;
+constexpr int kTileRowsPerWarp = 8;   // 16 warps x 8 rows = 128-row tiles
 constexpr int kRowBlocksPerWarp = kRowItemBlocks / (kThreads / 32);
 
 template <int Q>
@@ -61,22 +72,64 @@ __device__ __forceinline__ uint32_t encode1<DBUF_QUANT_INT8>(float v) {
     return uint32_t(uint8_t(int8_t(q)));
 }
 
-template <int Q>
-__device__ __forceinline__ uint32_t encode4(float4 v, float scale);
+// The divisor of one block: scale, its reciprocal, and whether the block takes
+// the IEEE division instructions (tiny scales) instead of the reciprocal step.
+struct Divisor {
+    float s, y;
+    bool exact;
+};
+
+__device__ __forceinline__ Divisor make_divisor(float scale) {
+    Divisor d;
+    d.s = scale;
+    d.y = __frcp_rn(scale);
+    d.exact = !(scale >= 0x1p-80f);
+    return d;
+}
+
+// x / d.s rounded to nearest even (see the header comment).  EXACT selects the
+// IEEE division instructions; callers branch on d.exact once per block so that
+// the per-element code holds only one of the two forms.
+template <bool EXACT>
+__device__ __forceinline__ float quot(float x, const Divisor &d) {
+    if (EXACT) return __fdiv_rn(x, d.s);
+    const float q = __fmul_rn(x, d.y);
+    const float r = __fmaf_rn(-q, d.s, x);
+    return copysignf(__fmaf_rn(r, d.y, q), x);
+}
+
+template <int Q, bool EXACT>
+__device__ __forceinline__ uint32_t encode4(float4 v, const Divisor &d);
 template <>
-__device__ __forceinline__ uint32_t encode4<DBUF_QUANT_E4M3>(float4 v, float scale) {
-    const float2 lo = make_float2(__fdiv_rn(v.x, scale), __fdiv_rn(v.y, scale));
-    const float2 hi = make_float2(__fdiv_rn(v.z, scale), __fdiv_rn(v.w, scale));
+__device__ __forceinline__ uint32_t encode4<DBUF_QUANT_E4M3, false>(float4 v, const Divisor &d) {
+    const float2 lo = make_float2(quot<false>(v.x, d), quot<false>(v.y, d));
+    const float2 hi = make_float2(quot<false>(v.z, d), quot<false>(v.w, d));
     const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
     const uint32_t b = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
     return (a & 0xFFFFu) | (b << 16);
 }
 template <>
-__device__ __forceinline__ uint32_t encode4<DBUF_QUANT_INT8>(float4 v, float scale) {
-    return encode1<DBUF_QUANT_INT8>(__fdiv_rn(v.x, scale)) |
-           (encode1<DBUF_QUANT_INT8>(__fdiv_rn(v.y, scale)) << 8) |
-           (encode1<DBUF_QUANT_INT8>(__fdiv_rn(v.z, scale)) << 16) |
-           (encode1<DBUF_QUANT_INT8>(__fdiv_rn(v.w, scale)) << 24);
+__device__ __forceinline__ uint32_t encode4<DBUF_QUANT_E4M3, true>(float4 v, const Divisor &d) {
+    const float2 lo = make_float2(quot<true>(v.x, d), quot<true>(v.y, d));
+    const float2 hi = make_float2(quot<true>(v.z, d), quot<true>(v.w, d));
+    const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
+    const uint32_t b = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
+    return (a & 0xFFFFu) | (b << 16);
+}
+template <bool EXACT>
+__device__ __forceinline__ uint32_t encode4_int8(float4 v, const Divisor &d) {
+    return encode1<DBUF_QUANT_INT8>(quot<EXACT>(v.x, d)) |
+           (encode1<DBUF_QUANT_INT8>(quot<EXACT>(v.y, d)) << 8) |
+           (encode1<DBUF_QUANT_INT8>(quot<EXACT>(v.z, d)) << 16) |
+           (encode1<DBUF_QUANT_INT8>(quot<EXACT>(v.w, d)) << 24);
+}
+template <>
+__device__ __forceinline__ uint32_t encode4<DBUF_QUANT_INT8, false>(float4 v, const Divisor &d) {
+    return encode4_int8<false>(v, d);
+}
+template <>
+__device__ __forceinline__ uint32_t encode4<DBUF_QUANT_INT8, true>(float4 v, const Divisor &d) {
+    return encode4_int8<true>(v, d);
 }
 
 __device__ __forceinline__ float abs_max4(float m, float4 v) {
@@ -110,9 +163,11 @@ __device__ __forceinline__ float quant_block_scalar(const float *x, uint8_t *y, 
     }
     amax = reduce_max(amax);
     const float scale = block_scale(amax, QParams<Q>::qmax);
+    const Divisor d = make_divisor(scale);
     for (int64_t i = tid; i < cnt; i += nthr) {
         const int64_t r = i / w, c = i % w;
-        y[r * cols + c] = uint8_t(encode1<Q>(__fdiv_rn(x[r * cols + c], scale)));
+        const float v = d.exact ? quot<true>(x[r * cols + c], d) : quot<false>(x[r * cols + c], d);
+        y[r * cols + c] = uint8_t(encode1<Q>(v));
     }
     return scale;
 }
@@ -130,7 +185,7 @@ __device__ __forceinline__ void tile_body(const QItem &it, const TensorDesc &d,
     const float *x = buf + d.buf_off + r0 * cols + c0;
     uint8_t *y = codes + d.buf_off + r0 * cols + c0;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const bool fast = h <= (kThreads / 32) * kTileRowsPerWarp && w <= 128 && (w & 3) == 0 &&
+    const bool fast = h <= kTileWarps * kTileRowsPerWarp && w <= 128 && (w & 3) == 0 &&
                       (cols & 3) == 0 && aligned_mod(x, 16) && aligned_mod(y, 4);
     float scale;
     if (fast) {
@@ -139,7 +194,7 @@ __device__ __forceinline__ void tile_body(const QItem &it, const TensorDesc &d,
         const bool col_ok = 4 * lane < w;
 #pragma unroll
         for (int k = 0; k < kTileRowsPerWarp; ++k) {
-            const int r = warp + k * (kThreads / 32);
+            const int r = warp + k * kTileWarps;
             v[k] = (r < h && col_ok) ? ld4(x + r * cols + 4 * lane) : make_float4(0.f, 0.f, 0.f, 0.f);
         }
 #pragma unroll
@@ -149,32 +204,44 @@ __device__ __forceinline__ void tile_body(const QItem &it, const TensorDesc &d,
         __syncthreads();
         amax = sh_max[0];
 #pragma unroll
-        for (int i = 1; i < kThreads / 32; ++i) amax = fmaxf(amax, sh_max[i]);
+        for (int i = 1; i < kTileWarps; ++i) amax = fmaxf(amax, sh_max[i]);
         scale = block_scale(amax, QParams<Q>::qmax);
+        const Divisor dv = make_divisor(scale);
+        if (!dv.exact) {
 #pragma unroll
-        for (int k = 0; k < kTileRowsPerWarp; ++k) {
-            const int r = warp + k * (kThreads / 32);
-            if (r < h && col_ok)
-                __stcs(reinterpret_cast<unsigned int *>(y + r * cols + 4 * lane), encode4<Q>(v[k], scale));
+            for (int k = 0; k < kTileRowsPerWarp; ++k) {
+                const int r = warp + k * kTileWarps;
+                if (r < h && col_ok)
+                    __stcs(reinterpret_cast<unsigned int *>(y + r * cols + 4 * lane),
+                           encode4<Q, false>(v[k], dv));
+            }
+        } else {
+#pragma unroll
+            for (int k = 0; k < kTileRowsPerWarp; ++k) {
+                const int r = warp + k * kTileWarps;
+                if (r < h && col_ok)
+                    __stcs(reinterpret_cast<unsigned int *>(y + r * cols + 4 * lane),
+                           encode4<Q, true>(v[k], dv));
+            }
         }
     } else {
-        scale = quant_block_scalar<Q>(x, y, cols, h, w, threadIdx.x, kThreads, [&](float m) {
+        scale = quant_block_scalar<Q>(x, y, cols, h, w, threadIdx.x, kTileThreads, [&](float m) {
             m = warp_max(m);
             if (lane == 0) sh_max[warp] = m;
             __syncthreads();
             float r = sh_max[0];
-            for (int i = 1; i < kThreads / 32; ++i) r = fmaxf(r, sh_max[i]);
+            for (int i = 1; i < kTileWarps; ++i) r = fmaxf(r, sh_max[i]);
             return r;
         });
     }
     if (threadIdx.x == 0) scales[d.scale_off + it.first] = scale;
 }
 
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kTileThreads, 2)
     quant_tile_kernel(const QItem *__restrict__ items, const TensorDesc *__restrict__ td,
                       const float *__restrict__ buf, uint8_t *__restrict__ codes,
                       float *__restrict__ scales) {
-    __shared__ float sh_max[kThreads / 32];
+    __shared__ float sh_max[kTileWarps];
     const QItem it = items[blockIdx.x];
     const TensorDesc d = td[it.tensor];
     if (d.quant == DBUF_QUANT_E4M3) tile_body<DBUF_QUANT_E4M3>(it, d, buf, codes, scales, sh_max);
@@ -217,8 +284,13 @@ __device__ __forceinline__ void row_body(const QItem &it, const TensorDesc &d,
             if (k >= it.count) continue;  // warp-uniform
             const float amax = warp_max(abs_max4(0.0f, v[j]));
             const float scale = block_scale(amax, QParams<Q>::qmax);
-            if (4 * lane < wid[j])
-                __stcs(reinterpret_cast<unsigned int *>(yt + boff[j] + 4 * lane), encode4<Q>(v[j], scale));
+            const Divisor dv = make_divisor(scale);
+            unsigned int *dst = reinterpret_cast<unsigned int *>(yt + boff[j] + 4 * lane);
+            if (!dv.exact) {
+                if (4 * lane < wid[j]) __stcs(dst, encode4<Q, false>(v[j], dv));
+            } else {
+                if (4 * lane < wid[j]) __stcs(dst, encode4<Q, true>(v[j], dv));
+            }
             if (lane == 0) scales[d.scale_off + it.first + k] = scale;
         }
     } else {
@@ -251,7 +323,7 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
                  void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     if (!p->tile_items.empty()) {
-        quant_tile_kernel<<<unsigned(p->tile_items.size()), kThreads, 0, st>>>(
+        quant_tile_kernel<<<unsigned(p->tile_items.size()), kTileThreads, 0, st>>>(
             p->dev.tile_items, p->dev.tensors, buf, codes, scales);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

@@ -104,7 +104,9 @@ class DBuffer:
     def workspace(self) -> torch.Tensor:
         nbytes = _c.dbuf_workspace_bytes(self.handle, _c.DBUF_OP_NORM_NONFINITE)
         if self._workspace is None or self._workspace.numel() < nbytes:
-            self._workspace = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            # zero-filled once: the norm's completion counters start at zero and
+            # every call leaves them at zero again
+            self._workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
         return self._workspace
 
     # -- group operators ---------------------------------------------------------

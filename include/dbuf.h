@@ -208,14 +208,19 @@ size_t dbuf_workspace_bytes(const dbuf_plan_t *plan, int32_t op);
  * L2 norm, and a flag for any non-finite value (inf or NaN) in any tensor range.
  * [veScale OpDispatcher: ragged norm handler and non-finite check handler;
  * PyTorch FSDP sharded gradient scaler and known limitations.]
- * Sums of squares are accumulated per chunk in fp32 and combined in fp64 in a
- * fixed order (deterministic, run to run); norms are returned in fp32.
+ * One launch: sums of squares are accumulated per chunk in fp32 and combined in
+ * fp64 in a fixed order by the last chunk of each tensor and then the last
+ * tensor to finish (deterministic, run to run); norms are returned in fp32.
+ * The workspace holds completion counters that must be zero when a call
+ * starts: zero-fill it once after allocating it (e.g. cudaMemset); every call
+ * returns the counters to zero before it finishes.
  * buf: device buffer of dtype (DBUF_F32 or DBUF_BF16).  Outputs are device
  * pointers: tensor_norms [n] floats, total_norm 1 float, nonfinite 1 int32
  * (0 or 1).  When the flag is 1 the norms are not meaningful.
  * workspace: caller-owned device scratch of at least
- * dbuf_workspace_bytes(plan, DBUF_OP_NORM_NONFINITE) bytes, 256-byte aligned;
- * it must not be shared by operations that may overlap on the GPU.
+ * dbuf_workspace_bytes(plan, DBUF_OP_NORM_NONFINITE) bytes, 256-byte aligned,
+ * zero-filled before its first use (see above); it must not be shared by
+ * operations that may overlap on the GPU.
  * Errors: DBUF_EINVAL (also for a too-small workspace), DBUF_ENOTUPLOADED,
  * DBUF_EDEVICE, DBUF_ECUDA.
  */
@@ -257,9 +262,12 @@ int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, 
  * device looks up the array's device address (once per device, with that
  * device current); make that first call before any stream capture.  All calls
  * share the one array: calls that may overlap on the GPU (other streams, other
- * host threads) race on it, so the caller must serialise them.  Nothing in the
- * scratch needs to start at zero; each call writes all it reads.  The call
- * allocates nothing (no cudaMalloc, cudaFree or allocating library routine).
+ * host threads) race on it, so the caller must serialise them.  The counters
+ * that must start at zero are zero when the library loads and every call
+ * returns them to zero before it finishes; everything else a call reads it
+ * writes first, so it does not depend on what the previous call left in the
+ * array.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
+ * library routine).
  * Arguments, outputs and other errors as for dbuf_norm_nonfinite.
  */
 #define DBUF_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)

@@ -344,3 +344,48 @@ def test_operators_on_a_side_stream(lib, oracle_lib):
     want = np.zeros(db.total, np.uint16)
     oracle_lib.pack(op, [f32(x) for x in src], want)
     assert_bits_equal(bf16_bits(buf), want, "pack on a side stream")
+
+
+def test_quant_quotient_stress(lib, oracle_lib):
+    """Blocks whose scales straddle 2^-80 (below it the kernel divides with the
+    IEEE instructions, above it from the block's reciprocal), subnormal and
+    signed-zero inputs, and inputs whose quotient by a non-trivial scale sits on
+    or next to an E4M3 midpoint or an INT8 half-integer."""
+    rng = np.random.default_rng(21)
+    mags = np.array([oracle_lib.e4m3_value(c) for c in range(127)])
+    mids = (mags[:-1] + mags[1:]) / 2
+    rows, cols = 64, 128
+    blocks = []
+    for amax in [1e-38, 2.0 ** -70 * 448, 2.0 ** -80 * 448 * 0.999, 2.0 ** -80 * 448 * 1.001,
+                 3.1e-3, 0.02, 1.7, 123.0, 3e30]:
+        for q, qmax, targets in [("e4m3", 448.0, mids), ("int8", 127.0,
+                                                         np.arange(-126.5, 127.0, 1.0))]:
+            s = np.float32(np.float32(amax) / np.float32(qmax))
+            t = rng.choice(targets, rows * cols)
+            x = (t * np.float64(s)).astype(np.float32)
+            k = rng.integers(-2, 3, x.size)
+            x = np.array([np.float32(v) if d == 0 else
+                          (np.nextafter(v, np.float32(np.inf * np.sign(d))) if abs(d) == 1 else
+                           np.nextafter(np.nextafter(v, np.float32(np.inf * np.sign(d))),
+                                        np.float32(np.inf * np.sign(d))))
+                          for v, d in zip(x, k)], np.float32)
+            x[:16] = np.array([0.0, -0.0, 1e-45, -1e-45, 1e-40, -3e-39, 2e-38, -2e-38] * 2,
+                              np.float32)
+            x = np.clip(x, -np.float32(amax), np.float32(amax))
+            x[16] = np.float32(amax)          # fixes the block's amax
+            blocks.append((q, x.reshape(rows, cols)))
+    for q in ("e4m3", "int8"):
+        data = [b for kind, b in blocks if kind == q]
+        qb = (rows, cols) if q == "e4m3" else (1, cols)
+        specs = [TensorSpec(f"b{i}", rows, cols, 0, qb, q) for i in range(len(data))]
+        op = oracle_lib.plan_specs(specs, 2, None, 16)
+        db = _db(specs, 2)
+        buf = torch.zeros(db.total, dtype=torch.float32, device=DEV)
+        for i, x in enumerate(data):
+            buf[db.offsets[i]:db.offsets[i] + x.size].copy_(torch.from_numpy(x.reshape(-1)))
+        codes = torch.full((db.total,), 0xAB, dtype=torch.uint8, device=DEV)
+        codes, scales = db.block_quant(buf, codes=codes)
+        wc = np.full(db.total, 0xAB, np.uint8)
+        ws = oracle_lib.block_quant(op, specs, f32(buf), wc)
+        assert_bits_equal(f32(scales), ws, f"{q} stress scales")
+        assert_bits_equal(codes.cpu().numpy(), wc, f"{q} stress codes")
