@@ -49,6 +49,23 @@ def _peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(x: float, device) -> float:
+    """The largest value of x over all ranks (the slowest rank's time); x itself
+    when not distributed."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank_step: float, ms_per_step: float, world: int) -> float:
+    """Whole-job GB/s: every rank (one independent replica per GPU) moves
+    bytes_per_rank_step per step; the step time is the slowest rank's."""
+    return world * bytes_per_rank_step / (ms_per_step / 1e3) / 1e9
+
+
 def _dist():
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -376,16 +393,13 @@ def _config_dict(stack, key):
 
 
 def _traffic_for(kernel_key):
-    """dram bytes per launch recorded from an ncu capture, if the kernel source
-    is unchanged since (profiles/dram_traffic.txt carries the source hash)."""
+    """dram bytes per launch recorded from an ncu capture (profiles/dram_traffic.txt),
+    or None if any source file of that kernel changed since (the record carries
+    the files' sha256 prefixes)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    src = {}
-    for f in os.listdir(os.path.join(ROOT, "fsdp_infra_gb300", "csrc")):
-        if f.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(ROOT, "fsdp_infra_gb300", "csrc", f), "rb") as fh:
-                src[f] = hashlib.sha256(fh.read()).hexdigest()[:16]
+    csrc = os.path.join(ROOT, "fsdp_infra_gb300", "csrc")
     with open(path) as f:
         for line in f:
             if line.startswith("#") or "=" not in line:
@@ -393,8 +407,13 @@ def _traffic_for(kernel_key):
             kv = dict(x.split("=", 1) for x in line.split())
             if kv.get("op") != kernel_key:
                 continue
-            if src.get(kv.get("file")) != kv.get("sha"):
-                return None
+            for name, sha in zip(kv["files"].split(","), kv["sha"].split(",")):
+                try:
+                    with open(os.path.join(csrc, name), "rb") as fh:
+                        if hashlib.sha256(fh.read()).hexdigest()[:16] != sha:
+                            return None
+                except OSError:
+                    return None
             return float(kv["bytes_per_launch"])
     return None
 
@@ -469,14 +488,9 @@ def run_ours(args):
     torch.cuda.synchronize()
     barrier()
     clock_info = clocks.stop()
-    elapsed_ms = t_start.elapsed_time(t_end)
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([elapsed_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        elapsed_ms = float(t.item())
+    elapsed_ms = max_over_ranks(t_start.elapsed_time(t_end), device)
     ms_per_step = elapsed_ms / args.steps
-    value = world * stack.bytes_per_step / (ms_per_step / 1e3) / 1e9
+    value = job_throughput(stack.bytes_per_step, ms_per_step, world)
     per_op = timers.totals_ms()
 
     # achieved for the dominant operator: algorithmic bytes of one launch on a
@@ -588,13 +602,8 @@ def run_e2e(stack, args, world):
     for _ in range(steps):
         step()
     torch.cuda.synchronize()
-    dt = time.perf_counter() - t0
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([dt], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        dt = float(t.item())
-    value = world * stack.bytes_per_step * steps / dt / 1e9
+    dt = max_over_ranks(time.perf_counter() - t0, device)
+    value = job_throughput(stack.bytes_per_step, 1e3 * dt / steps, world)
     return {"value": round(value, 1), "unit": "GB/s", "h2d_bytes_per_step": h2d,
             "d2h_bytes_per_step": d2h, "steps": steps,
             "ms_per_step": round(1000 * dt / steps, 3)}
