@@ -49,7 +49,13 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     const size_t b_c = align256(sizeof(dbuf::Chunk) * p->chunks.size());
     const size_t b_r = align256(sizeof(dbuf::QItem) * p->row_items.size());
     const size_t b_q = align256(sizeof(dbuf::QItem) * p->tile_items.size());
-    const size_t bytes = b_t + b_c + b_r + b_q + 256;
+    const size_t b_p = align256(sizeof(dbuf::TileItem) * p->pipe_items.size());
+    const size_t bytes = b_t + b_c + b_r + b_q + b_p + 256;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int prep = dbuf::prepare_quant_kernels();
+    if (prep != int(cudaSuccess)) return cuda_fail(cudaError_t(prep));
     void *base = nullptr;
     e = cudaMalloc(&base, bytes);
     if (e != cudaSuccess) {
@@ -65,16 +71,25 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     t.chunks = reinterpret_cast<dbuf::Chunk *>(c + b_t);
     t.row_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c);
     t.tile_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c + b_r);
+    t.pipe_items = reinterpret_cast<dbuf::TileItem *>(c + b_t + b_c + b_r + b_q);
+    t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p);
+    t.num_sms = sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    e = cudaMemsetAsync(t.status, 0, sizeof(int32_t), st);
+    if (e != cudaSuccess) {
+        cudaFree(base);
+        return cuda_fail(e);
+    }
     struct Piece {
         void *dst;
         const void *src;
         size_t n;
-    } pieces[4] = {
+    } pieces[5] = {
         {t.tensors, p->tdesc.data(), sizeof(dbuf::TensorDesc) * p->tdesc.size()},
         {t.chunks, p->chunks.data(), sizeof(dbuf::Chunk) * p->chunks.size()},
         {t.row_items, p->row_items.data(), sizeof(dbuf::QItem) * p->row_items.size()},
         {t.tile_items, p->tile_items.data(), sizeof(dbuf::QItem) * p->tile_items.size()},
+        {t.pipe_items, p->pipe_items.data(), sizeof(dbuf::TileItem) * p->pipe_items.size()},
     };
     for (const Piece &pc : pieces) {
         if (!pc.n) continue;
@@ -153,4 +168,22 @@ extern "C" int dbuf_block_quant(const dbuf_plan_t *p, const float *buf, uint8_t 
     if (rc) return rc;
     if (p->n_scales > 0 && (!buf || !codes || !scales)) return DBUF_EINVAL;
     return finish(dbuf::launch_quant(p, buf, codes, scales, stream));
+}
+
+extern "C" int dbuf_device_status(const dbuf_plan_t *p, int32_t *status, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!status) return DBUF_EINVAL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    int32_t v = 0;
+    cudaError_t e = cudaMemcpyAsync(&v, p->dev.status, sizeof(v), cudaMemcpyDeviceToHost, st);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) return cuda_fail(e);
+    if (v != 0) {
+        e = cudaMemsetAsync(p->dev.status, 0, sizeof(int32_t), st);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    *status = v;
+    return DBUF_OK;
 }

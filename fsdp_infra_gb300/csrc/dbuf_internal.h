@@ -50,14 +50,34 @@ struct QItem {
 };
 static_assert(sizeof(QItem) == 16, "QItem layout");
 
+// One quantisation tile for the pipelined tile kernel: block (bi, bj) of a
+// tensor whose tiles a 2-D tensor-memory-access copy can fetch (at most
+// 128 x 128 fp32, rows and tile widths multiples of 16 bytes, the tensor at a
+// 16-byte-aligned offset of a 16-byte-aligned buffer).  `slot` is the tensor's
+// index in the per-call table of tensor maps.
+struct TileItem {
+    int32_t tensor;
+    int32_t bi;
+    int32_t bj;
+    int32_t slot;
+};
+static_assert(sizeof(TileItem) == 16, "TileItem layout");
+
+constexpr int kPipeMaxRows = 128;
+constexpr int kPipeMaxCols = 128;
+constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch
+
 struct DeviceTables {
     TensorDesc *tensors = nullptr;
     Chunk *chunks = nullptr;
-    QItem *row_items = nullptr;   // blocks with qrows == 1
-    QItem *tile_items = nullptr;  // blocks with qrows > 1 (one block per item)
+    QItem *row_items = nullptr;      // blocks with qrows == 1
+    QItem *tile_items = nullptr;     // other blocks with qrows > 1 (one block per item)
+    TileItem *pipe_items = nullptr;  // tiles for the pipelined kernel
+    int32_t *status = nullptr;       // device status word (0, or DBUF_ETIMEOUT)
     void *base = nullptr;
     size_t bytes = 0;
     int device = -1;
+    int num_sms = 0;
 };
 
 // Launchers (one kernel launch over the whole group each; the norm adds a
@@ -74,6 +94,10 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
                  void *stream);
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p);
+
+// One-time per-device set-up of the quantisation kernels (shared memory
+// limits); called from dbuf_plan_upload.  Returns a cudaError_t value.
+int prepare_quant_kernels();
 
 // Keeps a cudaError_t for dbuf_last_cuda_error() (per host thread).
 void record_cuda_error(int e);
@@ -99,6 +123,8 @@ struct dbuf_plan {
     std::vector<dbuf::Chunk> chunks;
     std::vector<dbuf::QItem> row_items;
     std::vector<dbuf::QItem> tile_items;
+    std::vector<dbuf::TileItem> pipe_items;
+    std::vector<int32_t> pipe_tensors;  // slot -> tensor id
 
     bool uploaded = false;
     dbuf::DeviceTables dev;

@@ -31,6 +31,11 @@
 // Shapes outside the vector fast path (odd widths, unaligned rows, blocks
 // wider than 128 columns or taller than 128 rows) take a scalar two-pass path
 // in the same kernels.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "common.cuh"
 
 namespace dbuf {
@@ -146,7 +151,7 @@ __device__ __forceinline__ float4 ld4(const float *p) {
     return __ldcs(reinterpret_cast<const float4 *>(p));
 }
 
-__device__ __forceinline__ bool aligned_mod(const void *p, unsigned a) {
+__host__ __device__ __forceinline__ bool aligned_mod(const void *p, unsigned a) {
     return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }
 
@@ -248,6 +253,20 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     else tile_body<DBUF_QUANT_INT8>(it, d, buf, codes, scales, sh_max);
 }
 
+// The register-tile kernel over the pipelined list, for buffers that are not
+// 16-byte aligned (the rows then cannot be bulk-copied).
+__global__ void __launch_bounds__(kTileThreads, 2)
+    quant_tile_pipe_list_kernel(const TileItem *__restrict__ items,
+                                const TensorDesc *__restrict__ td, const float *__restrict__ buf,
+                                uint8_t *__restrict__ codes, float *__restrict__ scales) {
+    __shared__ float sh_max[kTileWarps];
+    const TileItem ti = items[blockIdx.x];
+    const TensorDesc d = td[ti.tensor];
+    const QItem it{int64_t(ti.bi) * d.nbc + ti.bj, ti.tensor, 1};
+    if (d.quant == DBUF_QUANT_E4M3) tile_body<DBUF_QUANT_E4M3>(it, d, buf, codes, scales, sh_max);
+    else tile_body<DBUF_QUANT_INT8>(it, d, buf, codes, scales, sh_max);
+}
+
 template <int Q>
 __device__ __forceinline__ void row_body(const QItem &it, const TensorDesc &d,
                                          const float *__restrict__ buf,
@@ -317,11 +336,292 @@ __global__ void __launch_bounds__(kThreads)
     else row_body<DBUF_QUANT_INT8>(it, d, buf, codes, scales);
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined tile kernel.  One 512-thread CTA per SM walks its tiles (item
+// blockIdx.x, blockIdx.x + gridDim.x, ...) through a ring of kPipeStages
+// shared-memory tile buffers.  One thread fetches a whole tile with a single
+// 2-D tensor-memory-access copy (cp.async.bulk.tensor, tensor map of that
+// tensor, zero fill past the tensor's edge) completing on the buffer's
+// mbarrier; all warps wait on it, pull the tile into registers (warp w holds
+// rows w, w+16, ...), and after the block-wide amax barrier the buffer is
+// refilled with the tile kPipeStages ahead while the codes are encoded and
+// stored.  With 3 buffers, two tiles stream in while one is encoded.
+// Every mbarrier wait is bounded: on expiry the CTA records DBUF_ETIMEOUT in
+// the plan's status word, waits (bounded again) for its own copies still in
+// flight, and returns.
+// ---------------------------------------------------------------------------
+constexpr int kPipeThreads = 512;
+constexpr int kPipeWarps = kPipeThreads / 32;
+constexpr int kPipeStages = 3;
+constexpr int kPipeStageBytes = kPipeMaxRows * kPipeMaxCols * 4;
+constexpr int kPipeRowsPerWarp = kPipeMaxRows / kPipeWarps;
+constexpr size_t kPipeSmemBytes = size_t(kPipeStages) * kPipeStageBytes + 1024 + 256;
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+struct TmaMaps {
+    CUtensorMap map[kPipeMaxTensors];
+};
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_fence_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n"
+        ".reg .pred p;\n"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        "selp.u32 %0, 1, 0, p;\n"
+        "}\n"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Waits for the phase of `parity` to complete, giving up after kWaitLimit tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    return false;
+}
+
+// The box of tensor map `map` at element coordinates (x = column, y = row)
+// into this CTA's shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y,
+                                            uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+
+struct PipeTile {
+    uint8_t *y;
+    int64_t cols;
+    int64_t scale_idx;
+    int h, w, quant, qrows, qcols, slot, x0, y0;
+};
+
+__device__ __forceinline__ PipeTile pipe_tile(const TileItem &it, const TensorDesc *__restrict__ td,
+                                              uint8_t *codes) {
+    const TensorDesc &d = td[it.tensor];
+    PipeTile g;
+    const int64_t r0 = int64_t(it.bi) * d.qrows, c0 = int64_t(it.bj) * d.qcols;
+    g.cols = d.cols;
+    g.h = int(imin64(d.qrows, d.rows - r0));
+    g.w = int(imin64(d.qcols, d.cols - c0));
+    g.y = codes + d.buf_off + r0 * d.cols + c0;
+    g.scale_idx = d.scale_off + int64_t(it.bi) * d.nbc + it.bj;
+    g.quant = d.quant;
+    g.qrows = d.qrows;
+    g.qcols = d.qcols;
+    g.slot = it.slot;
+    g.x0 = int(c0);
+    g.y0 = int(r0);
+    return g;
+}
+
+// One thread: expect the full box (edge tiles are zero-filled) and fetch it.
+__device__ __forceinline__ void pipe_issue(const PipeTile &g, const TmaMaps &maps, char *stage,
+                                           uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, uint32_t(g.qrows) * uint32_t(g.qcols) * 4u);
+    tma_load_2d(stage, &maps.map[g.slot], g.x0, g.y0, bar);
+}
+
+template <int Q>
+__device__ __forceinline__ void pipe_encode_store(const PipeTile &g, const float4 (&v)[kPipeRowsPerWarp],
+                                                  const Divisor &dv, int warp, int lane) {
+    const bool col_ok = 4 * lane < g.w;
+    if (!dv.exact) {
+#pragma unroll
+        for (int k = 0; k < kPipeRowsPerWarp; ++k) {
+            const int r = warp + k * kPipeWarps;
+            if (r < g.h && col_ok)
+                __stcs(reinterpret_cast<unsigned int *>(g.y + r * g.cols + 4 * lane),
+                       encode4<Q, false>(v[k], dv));
+        }
+    } else {
+#pragma unroll
+        for (int k = 0; k < kPipeRowsPerWarp; ++k) {
+            const int r = warp + k * kPipeWarps;
+            if (r < g.h && col_ok)
+                __stcs(reinterpret_cast<unsigned int *>(g.y + r * g.cols + 4 * lane),
+                       encode4<Q, true>(v[k], dv));
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kPipeThreads, 1)
+    quant_pipe_kernel(const __grid_constant__ TmaMaps maps, const TileItem *__restrict__ items,
+                      int nitems, const TensorDesc *__restrict__ td, uint8_t *__restrict__ codes,
+                      float *__restrict__ scales, int32_t *__restrict__ status) {
+    extern __shared__ unsigned char smem_raw[];
+    // tensor copies land at 1024-byte-aligned buffers
+    char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stages + size_t(kPipeStages) * kPipeStageBytes);
+    float *sh_max = reinterpret_cast<float *>(bars + kPipeStages);  // [2][kPipeWarps]
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int G = gridDim.x;
+
+    if (tid == 0) {
+        for (int s = 0; s < kPipeStages; ++s) mbar_init(&bars[s], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    // Prologue: the first kPipeStages tiles of this CTA.
+    int issued = 0;  // tiles of this CTA whose copies were issued
+    for (int s = 0; s < kPipeStages; ++s) {
+        const int i = blockIdx.x + s * G;
+        if (i >= nitems) break;
+        if (tid == 0) pipe_issue(pipe_tile(items[i], td, codes), maps, stages + s * kPipeStageBytes,
+                                 &bars[s]);
+        ++issued;
+    }
+
+    int k = 0;  // index of the tile of this CTA being processed
+    bool failed = false;
+    for (int i = blockIdx.x; i < nitems; i += G, ++k) {
+        const int s = k % kPipeStages;
+        const uint32_t parity = uint32_t(k / kPipeStages) & 1u;
+        const PipeTile g = pipe_tile(items[i], td, codes);
+        const bool got = mbar_wait_bounded(&bars[s], parity);
+
+        const float *st = reinterpret_cast<const float *>(stages + s * kPipeStageBytes);
+        const bool col_ok = 4 * lane < g.w;
+        float4 v[kPipeRowsPerWarp];
+        float amax = 0.0f;
+#pragma unroll
+        for (int r8 = 0; r8 < kPipeRowsPerWarp; ++r8) {
+            const int r = warp + r8 * kPipeWarps;
+            v[r8] = (r < g.h && col_ok)
+                        ? *reinterpret_cast<const float4 *>(st + r * g.qcols + 4 * lane)
+                        : make_float4(0.f, 0.f, 0.f, 0.f);
+            amax = abs_max4(amax, v[r8]);
+        }
+        amax = warp_max(amax);
+        if (lane == 0) sh_max[(k & 1) * kPipeWarps + warp] = amax;
+        // Every thread has its rows in registers: the buffer may be refilled.
+        if (__syncthreads_or(!got)) {
+            failed = true;
+            break;
+        }
+        const int inext = i + kPipeStages * G;
+        if (inext < nitems) {
+            if (tid == 0) pipe_issue(pipe_tile(items[inext], td, codes), maps,
+                                     stages + s * kPipeStageBytes, &bars[s]);
+            ++issued;
+        }
+        amax = sh_max[(k & 1) * kPipeWarps];
+#pragma unroll
+        for (int w = 1; w < kPipeWarps; ++w) amax = fmaxf(amax, sh_max[(k & 1) * kPipeWarps + w]);
+        if (g.quant == DBUF_QUANT_E4M3) {
+            const float scale = block_scale(amax, QParams<DBUF_QUANT_E4M3>::qmax);
+            pipe_encode_store<DBUF_QUANT_E4M3>(g, v, make_divisor(scale), warp, lane);
+            if (tid == 0) scales[g.scale_idx] = scale;
+        } else {
+            const float scale = block_scale(amax, QParams<DBUF_QUANT_INT8>::qmax);
+            pipe_encode_store<DBUF_QUANT_INT8>(g, v, make_divisor(scale), warp, lane);
+            if (tid == 0) scales[g.scale_idx] = scale;
+        }
+    }
+    if (failed && tid == 0) {
+        atomicExch(status, DBUF_ETIMEOUT);
+        // Copies of tiles k .. issued-1 may still be in flight into this CTA's
+        // shared memory: wait for them (bounded) before the CTA exits.
+        for (int j = k; j < issued; ++j)
+            (void)mbar_wait_bounded(&bars[j % kPipeStages], uint32_t(j / kPipeStages) & 1u);
+    }
+}
+
+// Host: the tensor-map encoder, looked up once from the driver.
+std::mutex g_encode_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+}  // namespace
+
+int prepare_quant_kernels() {
+    cudaError_t e = cudaFuncSetAttribute(quant_pipe_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kPipeSmemBytes));
+    if (e != cudaSuccess) return int(e);
+    std::lock_guard<std::mutex> lock(g_encode_mutex);
+    if (!g_encode) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                             &q);
+        if (e != cudaSuccess) return int(e);
+        if (q != cudaDriverEntryPointSuccess || !fn) return int(cudaErrorNotSupported);
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    return int(cudaSuccess);
+}
+
+namespace {
+
+// Tensor maps of the pipelined tensors of `p` over the buffer `buf` (one 2-D
+// map per tensor: columns x rows, row pitch cols*4 bytes, box qcols x qrows).
+bool encode_maps(const dbuf_plan_t *p, const float *buf, TmaMaps *maps) {
+    if (!g_encode) return false;
+    for (size_t slot = 0; slot < p->pipe_tensors.size(); ++slot) {
+        const TensorDesc &d = p->tdesc[p->pipe_tensors[slot]];
+        const cuuint64_t dims[2] = {cuuint64_t(d.cols), cuuint64_t(d.rows)};
+        const cuuint64_t strides[1] = {cuuint64_t(d.cols) * 4u};
+        const cuuint32_t box[2] = {cuuint32_t(d.qcols), cuuint32_t(d.qrows)};
+        const cuuint32_t estr[2] = {1, 1};
+        void *base = const_cast<float *>(buf + d.buf_off);
+        const CUresult r = g_encode(&maps->map[slot], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
+                                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return false;
+    }
+    return true;
+}
+
 }  // namespace
 
 int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *scales,
                  void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // Pipelined tiles need 16-byte aligned rows: a 16-byte-aligned fp32 buffer
+    // and 4-byte-aligned codes (the plan checked the offsets and widths).
+    bool pipe_ok = !p->pipe_items.empty() && aligned_mod(buf, 16) && aligned_mod(codes, 4);
+    TmaMaps maps;
+    if (pipe_ok) pipe_ok = encode_maps(p, buf, &maps);
+    if (pipe_ok) {
+        const int n = int(p->pipe_items.size());
+        const int grid = n < p->dev.num_sms ? n : p->dev.num_sms;
+        quant_pipe_kernel<<<grid, kPipeThreads, kPipeSmemBytes, st>>>(
+            maps, p->dev.pipe_items, n, p->dev.tensors, codes, scales, p->dev.status);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    } else if (!p->pipe_items.empty()) {
+        quant_tile_pipe_list_kernel<<<unsigned(p->pipe_items.size()), kTileThreads, 0, st>>>(
+            p->dev.pipe_items, p->dev.tensors, buf, codes, scales);
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
     if (!p->tile_items.empty()) {
         quant_tile_kernel<<<unsigned(p->tile_items.size()), kTileThreads, 0, st>>>(
             p->dev.tile_items, p->dev.tensors, buf, codes, scales);

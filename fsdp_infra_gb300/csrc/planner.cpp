@@ -218,6 +218,8 @@ void build_tables(dbuf_plan_t *p) {
     p->chunks.clear();
     p->row_items.clear();
     p->tile_items.clear();
+    p->pipe_items.clear();
+    p->pipe_tensors.clear();
     int64_t s_off = 0;
     for (int32_t t = 0; t < n; ++t) {
         const dbuf_tensor_spec &s = p->specs[t];
@@ -244,7 +246,23 @@ void build_tables(dbuf_plan_t *p) {
                     p->row_items.push_back(
                         QItem{b, t, int32_t(std::min<int64_t>(dbuf::kRowItemBlocks, nb - b))});
             } else {
-                for (int64_t b = 0; b < nb; ++b) p->tile_items.push_back(QItem{b, t, 1});
+                // Tiles a 2-D tensor map can fetch (rows and tile widths multiples of
+                // 16 bytes at a 16-byte-aligned tensor offset) go to the pipelined
+                // kernel, for the first kPipeMaxTensors such tensors; the rest to the
+                // register-tile kernel.
+                const bool pipe = d.qrows <= dbuf::kPipeMaxRows && d.qcols <= dbuf::kPipeMaxCols &&
+                                  d.qcols % 4 == 0 && s.cols % 4 == 0 && d.buf_off % 4 == 0 &&
+                                  s.rows < (int64_t(1) << 31) && s.cols < (int64_t(1) << 31) &&
+                                  p->pipe_tensors.size() < size_t(dbuf::kPipeMaxTensors);
+                const int32_t slot = pipe ? int32_t(p->pipe_tensors.size()) : -1;
+                if (pipe) p->pipe_tensors.push_back(t);
+                for (int64_t b = 0; b < nb; ++b) {
+                    if (pipe)
+                        p->pipe_items.push_back(
+                            dbuf::TileItem{t, int32_t(b / d.nbc), int32_t(b % d.nbc), slot});
+                    else
+                        p->tile_items.push_back(QItem{b, t, 1});
+                }
             }
             s_off += nb;
         }
@@ -327,7 +345,7 @@ extern "C" int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
         for (int k = 0; k <= m; ++k) p->bounds[k] = S * c[k];
         build_tables(p);
         if (p->chunks.size() > size_t(INT32_MAX) || p->tile_items.size() > size_t(INT32_MAX) ||
-            p->row_items.size() > size_t(INT32_MAX)) {
+            p->row_items.size() > size_t(INT32_MAX) || p->pipe_items.size() > size_t(INT32_MAX)) {
             delete p;
             return DBUF_ERANGE;
         }

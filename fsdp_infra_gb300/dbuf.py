@@ -43,7 +43,7 @@ _QUANT = {None: DBUF_QUANT_NONE, "none": DBUF_QUANT_NONE, "e4m3": DBUF_QUANT_E4M
 EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
-           "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_device_status", "dbuf_strerror", "dbuf_last_cuda_error")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -103,6 +103,8 @@ def _lib_handle():
         L.dbuf_norm_nonfinite_noalloc.restype = ctypes.c_int
         L.dbuf_block_quant.argtypes = [P, P, P, P, P]
         L.dbuf_block_quant.restype = ctypes.c_int
+        L.dbuf_device_status.argtypes = [P, P, P]
+        L.dbuf_device_status.restype = ctypes.c_int
         L.dbuf_strerror.argtypes = [ctypes.c_int]
         L.dbuf_strerror.restype = ctypes.c_char_p
         L.dbuf_last_cuda_error.argtypes = []
@@ -206,6 +208,13 @@ def dbuf_norm_nonfinite_noalloc(plan: int, buf: int, dtype: int, tensor_norms: i
 
 def dbuf_block_quant(plan: int, buf: int, codes: int, scales: int, stream: int = 0) -> None:
     _check(_lib_handle().dbuf_block_quant(plan, buf, codes, scales, stream), "dbuf_block_quant")
+
+
+def dbuf_device_status(plan: int, stream: int = 0) -> int:
+    """Reads and clears the plan's device status word (0 or DBUF_ETIMEOUT)."""
+    v = ctypes.c_int32()
+    _check(_lib_handle().dbuf_device_status(plan, ctypes.byref(v), stream), "dbuf_device_status")
+    return v.value
 
 
 def dbuf_strerror(code: int) -> str:

@@ -57,7 +57,7 @@ extern "C" {
 #define DBUF_ENOMEM (-2)       /* host or device allocation failed */
 #define DBUF_ECUDA (-3)        /* a CUDA call or launch failed */
 #define DBUF_ENOTUPLOADED (-4) /* operator called on a plan not yet uploaded */
-#define DBUF_ETIMEOUT (-5)     /* reserved: a bounded device-side wait gave up */
+#define DBUF_ETIMEOUT (-5)     /* a bounded device-side wait gave up (dbuf_device_status) */
 #define DBUF_EDEVICE (-6)      /* current device differs from the plan's device */
 #define DBUF_ERANGE (-7)       /* a size exceeds what the call supports */
 
@@ -146,7 +146,9 @@ int dbuf_plan_query(const dbuf_plan_t *plan, int64_t *S, int64_t *total, int64_t
  * dbuf_plan_upload -- copies the plan's descriptor tables (tensor table, chunk
  * table, quantisation work lists) to the current device: the persistent
  * address mapping of [veScale-FSDP §5 DBuffer, zero-copy access].  Allocates
- * device memory owned by the plan and waits for the copies on `stream`.
+ * device memory owned by the plan (the tables and a status word), sets the
+ * shared-memory limit of the pipelined quantisation kernel on this device, and
+ * waits for the copies on `stream`.
  * Uploading twice on the same device is a no-op.
  * Errors: DBUF_EINVAL, DBUF_ENOMEM, DBUF_ECUDA, DBUF_EDEVICE (already uploaded
  * to another device).
@@ -240,7 +242,10 @@ int dbuf_norm_nonfinite(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
  * `total` bytes, same layout; bytes outside quantised tensors are untouched.
  * scales: device fp32 array of n_scales entries, tensor by tensor in row-major
  * block order starting at scale_offsets[t].  Inputs with inf/NaN give
- * unspecified codes.
+ * unspecified codes.  With a 16-byte-aligned buf and 4-byte-aligned codes,
+ * 2-D tiles of at most 128 x 128 whose rows are 16-byte multiples stream
+ * through shared memory by bulk copies (one persistent CTA per SM); other
+ * tiles and unaligned buffers take a register-tile kernel with equal results.
  * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
  */
 int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, float *scales,
@@ -274,6 +279,17 @@ int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, 
 int dbuf_norm_nonfinite_noalloc(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
                                 float *tensor_norms, float *total_norm, int32_t *nonfinite,
                                 void *stream);
+
+/*
+ * dbuf_device_status -- reads and clears the plan's device status word: 0, or
+ * DBUF_ETIMEOUT if a kernel of this plan gave up a bounded device-side wait
+ * (the pipelined block-quantisation kernel waits on shared-memory barriers for
+ * its bulk copies; on expiry it records the status and returns instead of
+ * hanging, and the affected codes are not valid).  Enqueues the read on
+ * `stream` and waits for it.  *status receives the value.
+ * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_device_status(const dbuf_plan_t *plan, int32_t *status, void *stream);
 
 /* dbuf_strerror -- static description of a return code. */
 const char *dbuf_strerror(int code);

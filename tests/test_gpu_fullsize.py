@@ -101,6 +101,8 @@ def sampled_group_parity(oracle_lib, op, w, gi, sample):
             so = int(q_offsets[t])
             assert_bits_equal(f32(scales[so:so + ws.size]), ws, f"{w.key} scales t{t}")
             assert_bits_equal(codes[o:o + k].cpu().numpy(), wc, f"{w.key} codes t{t}")
+    from fsdp_infra_gb300 import dbuf
+    assert dbuf.dbuf_device_status(db.handle) == 0
     del grad, acc, buf16, dst, codes
     torch.cuda.empty_cache()
 

@@ -118,6 +118,8 @@ def full_group_parity(oracle_lib, specs, m, units, align, *, param_fn, grad_fn, 
         assert db.n_scales == want_scales.size
         assert_bits_equal(f32(scales), want_scales, "scales")
         assert_bits_equal(codes.cpu().numpy(), want_codes, "codes")
+    from fsdp_infra_gb300 import dbuf
+    assert dbuf.dbuf_device_status(db.handle) == 0
     return db, op
 
 
@@ -389,3 +391,27 @@ def test_quant_quotient_stress(lib, oracle_lib):
         ws = oracle_lib.block_quant(op, specs, f32(buf), wc)
         assert_bits_equal(f32(scales), ws, f"{q} stress scales")
         assert_bits_equal(codes.cpu().numpy(), wc, f"{q} stress codes")
+
+
+def test_quant_unaligned_buffers_and_status(lib, oracle_lib):
+    """Buffers that are not 16-byte aligned (fp32 input offset by one element,
+    codes offset by one byte) cannot stream rows by bulk copy: the register-tile
+    path must give the same codes; the device status stays clear."""
+    specs = [TensorSpec("a", 256, 384, 128, (128, 128), "e4m3"),
+             TensorSpec("v", 100, 1, 1),
+             TensorSpec("b", 200, 136, 128, (128, 128), "int8")]
+    op = oracle_lib.plan_specs(specs, 2, None, 16)
+    db = _db(specs, 2)
+    gen = torch.Generator().manual_seed(17)
+    host = (torch.randn(db.total, generator=gen) * 0.05).to(torch.float32)
+    want_c = np.full(db.total, 0x5A, np.uint8)
+    want_s = oracle_lib.block_quant(op, specs, host.numpy().copy(), want_c)
+    for fshift, cshift in [(0, 0), (1, 0), (0, 1), (1, 3)]:
+        fb = torch.zeros(db.total + 4, dtype=torch.float32, device=DEV)
+        fb[fshift:fshift + db.total].copy_(host)
+        cb = torch.full((db.total + 4,), 0x5A, dtype=torch.uint8, device=DEV)
+        codes, scales = db.block_quant(fb[fshift:fshift + db.total],
+                                       codes=cb[cshift:cshift + db.total])
+        assert_bits_equal(f32(scales), want_s, f"scales shift {fshift},{cshift}")
+        assert_bits_equal(codes.cpu().numpy(), want_c, f"codes shift {fshift},{cshift}")
+    assert lib.dbuf_device_status(db.handle) == 0
