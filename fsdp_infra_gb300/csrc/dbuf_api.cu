@@ -47,7 +47,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
 
     const size_t b_t = align256(sizeof(dbuf::TensorDesc) * p->tdesc.size());
     const size_t b_c = align256(sizeof(dbuf::Chunk) * p->chunks.size());
-    const size_t b_r = align256(sizeof(dbuf::QItem) * p->row_items.size());
+    const size_t b_r = align256(sizeof(dbuf::RowItem) * p->row_items.size());
     const size_t b_q = align256(sizeof(dbuf::QItem) * p->tile_items.size());
     const size_t b_p = align256(sizeof(dbuf::TileItem) * p->pipe_items.size());
     const size_t bytes = b_t + b_c + b_r + b_q + b_p + 256;
@@ -69,7 +69,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     t.device = dev;
     t.tensors = reinterpret_cast<dbuf::TensorDesc *>(c);
     t.chunks = reinterpret_cast<dbuf::Chunk *>(c + b_t);
-    t.row_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c);
+    t.row_items = reinterpret_cast<dbuf::RowItem *>(c + b_t + b_c);
     t.tile_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c + b_r);
     t.pipe_items = reinterpret_cast<dbuf::TileItem *>(c + b_t + b_c + b_r + b_q);
     t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p);
@@ -87,7 +87,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     } pieces[5] = {
         {t.tensors, p->tdesc.data(), sizeof(dbuf::TensorDesc) * p->tdesc.size()},
         {t.chunks, p->chunks.data(), sizeof(dbuf::Chunk) * p->chunks.size()},
-        {t.row_items, p->row_items.data(), sizeof(dbuf::QItem) * p->row_items.size()},
+        {t.row_items, p->row_items.data(), sizeof(dbuf::RowItem) * p->row_items.size()},
         {t.tile_items, p->tile_items.data(), sizeof(dbuf::QItem) * p->tile_items.size()},
         {t.pipe_items, p->pipe_items.data(), sizeof(dbuf::TileItem) * p->pipe_items.size()},
     };

@@ -15,7 +15,7 @@ namespace dbuf {
 constexpr int64_t kChunkElems = 16384;
 
 // Blocks per work item of the row-block (1 x qc) quantisation kernel.
-constexpr int32_t kRowItemBlocks = 32;
+constexpr int32_t kRowItemBlocks = 64;
 
 // One tensor of the group, as the kernels see it (64 bytes).
 struct TensorDesc {
@@ -50,6 +50,16 @@ struct QItem {
 };
 static_assert(sizeof(QItem) == 16, "QItem layout");
 
+// A run of `count` consecutive 1 x qc blocks (row-major block order) of one
+// tensor, starting at block column bj0 of block row bi0.
+struct RowItem {
+    int32_t tensor;
+    int32_t bi0;
+    int32_t bj0;
+    int32_t count;
+};
+static_assert(sizeof(RowItem) == 16, "RowItem layout");
+
 // One quantisation tile for the pipelined tile kernel: block (bi, bj) of a
 // tensor whose tiles a 2-D tensor-memory-access copy can fetch (at most
 // 128 x 128 fp32, rows and tile widths multiples of 16 bytes, the tensor at a
@@ -70,7 +80,7 @@ constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch
 struct DeviceTables {
     TensorDesc *tensors = nullptr;
     Chunk *chunks = nullptr;
-    QItem *row_items = nullptr;      // blocks with qrows == 1
+    RowItem *row_items = nullptr;    // blocks with qrows == 1
     QItem *tile_items = nullptr;     // other blocks with qrows > 1 (one block per item)
     TileItem *pipe_items = nullptr;  // tiles for the pipelined kernel
     int32_t *status = nullptr;       // device status word (0, or DBUF_ETIMEOUT)
@@ -121,7 +131,7 @@ struct dbuf_plan {
 
     std::vector<dbuf::TensorDesc> tdesc;
     std::vector<dbuf::Chunk> chunks;
-    std::vector<dbuf::QItem> row_items;
+    std::vector<dbuf::RowItem> row_items;
     std::vector<dbuf::QItem> tile_items;
     std::vector<dbuf::TileItem> pipe_items;
     std::vector<int32_t> pipe_tensors;  // slot -> tensor id

@@ -44,7 +44,6 @@ namespace {
 constexpr int kTileThreads = 512;     // one CTA per tile
 constexpr int kTileWarps = kTileThreads / 32;
 constexpr int kTileRowsPerWarp = 8;   // 16 warps x 8 rows = 128-row tiles
-constexpr int kRowBlocksPerWarp = kRowItemBlocks / (kThreads / 32);
 
 template <int Q>
 struct QParams;
@@ -267,70 +266,102 @@ __global__ void __launch_bounds__(kTileThreads, 2)
     else tile_body<DBUF_QUANT_INT8>(it, d, buf, codes, scales, sh_max);
 }
 
+// Row blocks: 8 lanes per 1 x qc block (qc <= 128), each lane holding up to 4
+// float4 (16 elements) of it, so a warp covers 4 blocks and a CTA 32 blocks per
+// round; a thread keeps both rounds of its item in flight before reducing.
+// The block amax is a 3-level xor shuffle inside the 8-lane group.
+constexpr int kRowLanes = 8;
+constexpr int kRowGroups = kThreads / kRowLanes;
+constexpr int kRowRounds = kRowItemBlocks / kRowGroups;
+constexpr int kRowVecs = 128 / 4 / kRowLanes;  // float4 per lane per block
+
 template <int Q>
-__device__ __forceinline__ void row_body(const QItem &it, const TensorDesc &d,
+__device__ __forceinline__ void row_body(const RowItem &it, const TensorDesc &d,
                                          const float *__restrict__ buf,
                                          uint8_t *__restrict__ codes,
                                          float *__restrict__ scales) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t cols = d.cols;
     const float *xt = buf + d.buf_off;
     uint8_t *yt = codes + d.buf_off;
+    const uint32_t nbc = uint32_t(d.nbc);
     const bool fast = d.qcols <= 128 && (d.qcols & 3) == 0 && (cols & 3) == 0 &&
                       aligned_mod(xt, 16) && aligned_mod(yt, 4);
     if (fast) {
-        float4 v[kRowBlocksPerWarp];
-        int64_t boff[kRowBlocksPerWarp];
-        int wid[kRowBlocksPerWarp];
+        const int grp = threadIdx.x / kRowLanes, gl = threadIdx.x % kRowLanes;
+        float4 v[kRowRounds][kRowVecs];
+        int64_t off[kRowRounds], sidx[kRowRounds];
+        int wid[kRowRounds];
 #pragma unroll
-        for (int j = 0; j < kRowBlocksPerWarp; ++j) {
-            const int k = warp + j * (kThreads / 32);
+        for (int j = 0; j < kRowRounds; ++j) {
+            const int k = grp + j * kRowGroups;
             wid[j] = 0;
-            boff[j] = 0;
-            v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+            off[j] = 0;
+            sidx[j] = 0;
             if (k < it.count) {
-                const int64_t b = it.first + k;
-                const int64_t bi = b / d.nbc, bj = b % d.nbc;
+                const uint32_t t = uint32_t(it.bj0) + uint32_t(k);
+                const int64_t bi = int64_t(it.bi0) + t / nbc, bj = t % nbc;
                 const int64_t c0 = bj * d.qcols;
                 wid[j] = int(imin64(d.qcols, cols - c0));
-                boff[j] = bi * cols + c0;
-                if (4 * lane < wid[j]) v[j] = ld4(xt + boff[j] + 4 * lane);
+                off[j] = bi * cols + c0;
+                sidx[j] = d.scale_off + bi * d.nbc + bj;
+            }
+#pragma unroll
+            for (int u = 0; u < kRowVecs; ++u) {
+                const int f = 4 * (gl + u * kRowLanes);
+                v[j][u] = f < wid[j] ? ld4(xt + off[j] + f) : make_float4(0.f, 0.f, 0.f, 0.f);
             }
         }
 #pragma unroll
-        for (int j = 0; j < kRowBlocksPerWarp; ++j) {
-            const int k = warp + j * (kThreads / 32);
-            if (k >= it.count) continue;  // warp-uniform
-            const float amax = warp_max(abs_max4(0.0f, v[j]));
+        for (int j = 0; j < kRowRounds; ++j) {
+            float amax = 0.0f;
+#pragma unroll
+            for (int u = 0; u < kRowVecs; ++u) amax = abs_max4(amax, v[j][u]);
+            // all lanes take part: groups past the item's end reduce zeros
+#pragma unroll
+            for (int o = kRowLanes / 2; o > 0; o >>= 1)
+                amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+            if (wid[j] == 0) continue;
             const float scale = block_scale(amax, QParams<Q>::qmax);
             const Divisor dv = make_divisor(scale);
-            unsigned int *dst = reinterpret_cast<unsigned int *>(yt + boff[j] + 4 * lane);
             if (!dv.exact) {
-                if (4 * lane < wid[j]) __stcs(dst, encode4<Q, false>(v[j], dv));
+#pragma unroll
+                for (int u = 0; u < kRowVecs; ++u) {
+                    const int f = 4 * (gl + u * kRowLanes);
+                    if (f < wid[j])
+                        __stcs(reinterpret_cast<unsigned int *>(yt + off[j] + f),
+                               encode4<Q, false>(v[j][u], dv));
+                }
             } else {
-                if (4 * lane < wid[j]) __stcs(dst, encode4<Q, true>(v[j], dv));
+#pragma unroll
+                for (int u = 0; u < kRowVecs; ++u) {
+                    const int f = 4 * (gl + u * kRowLanes);
+                    if (f < wid[j])
+                        __stcs(reinterpret_cast<unsigned int *>(yt + off[j] + f),
+                               encode4<Q, true>(v[j][u], dv));
+                }
             }
-            if (lane == 0) scales[d.scale_off + it.first + k] = scale;
+            if (gl == 0) scales[sidx[j]] = scale;
         }
     } else {
+        const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
         for (int k = warp; k < it.count; k += kThreads / 32) {
-            const int64_t b = it.first + k;
-            const int64_t bi = b / d.nbc, bj = b % d.nbc;
+            const uint32_t t = uint32_t(it.bj0) + uint32_t(k);
+            const int64_t bi = int64_t(it.bi0) + t / nbc, bj = t % nbc;
             const int64_t c0 = bj * d.qcols;
             const int w = int(imin64(d.qcols, cols - c0));
             const float scale = quant_block_scalar<Q>(
                 xt + bi * cols + c0, yt + bi * cols + c0, cols, 1, w, lane, 32,
                 [](float m) { return warp_max(m); });
-            if (lane == 0) scales[d.scale_off + b] = scale;
+            if (lane == 0) scales[d.scale_off + bi * d.nbc + bj] = scale;
         }
     }
 }
 
 __global__ void __launch_bounds__(kThreads)
-    quant_row_kernel(const QItem *__restrict__ items, const TensorDesc *__restrict__ td,
+    quant_row_kernel(const RowItem *__restrict__ items, const TensorDesc *__restrict__ td,
                      const float *__restrict__ buf, uint8_t *__restrict__ codes,
                      float *__restrict__ scales) {
-    const QItem it = items[blockIdx.x];
+    const RowItem it = items[blockIdx.x];
     const TensorDesc d = td[it.tensor];
     if (d.quant == DBUF_QUANT_E4M3) row_body<DBUF_QUANT_E4M3>(it, d, buf, codes, scales);
     else row_body<DBUF_QUANT_INT8>(it, d, buf, codes, scales);

@@ -196,6 +196,9 @@ int validate(const dbuf_tensor_spec *specs, int32_t n, int32_t m, const int32_t 
         const dbuf_tensor_spec &s = specs[t];
         if (s.rows < 0 || s.cols < 0 || s.gran_rows < 0 || s.reserved != 0) return DBUF_EINVAL;
         if (s.rows > kMaxElems || s.cols > kMaxElems) return DBUF_ERANGE;
+        // block rows and block columns are indexed with 32-bit integers
+        if (s.quant != DBUF_QUANT_NONE && (s.rows >= (int64_t(1) << 31) || s.cols >= (int64_t(1) << 31)))
+            return DBUF_ERANGE;
         if (s.cols > 0 && s.rows > kMaxElems / s.cols) return DBUF_ERANGE;
         const int64_t numel = s.rows * s.cols;
         if (numel > kMaxElems - E) return DBUF_ERANGE;
@@ -243,8 +246,9 @@ void build_tables(dbuf_plan_t *p) {
             const int64_t nb = nbr * d.nbc;
             if (d.qrows == 1) {
                 for (int64_t b = 0; b < nb; b += dbuf::kRowItemBlocks)
-                    p->row_items.push_back(
-                        QItem{b, t, int32_t(std::min<int64_t>(dbuf::kRowItemBlocks, nb - b))});
+                    p->row_items.push_back(dbuf::RowItem{
+                        t, int32_t(b / d.nbc), int32_t(b % d.nbc),
+                        int32_t(std::min<int64_t>(dbuf::kRowItemBlocks, nb - b))});
             } else {
                 // Tiles a 2-D tensor map can fetch (rows and tile widths multiples of
                 // 16 bytes at a 16-byte-aligned tensor offset) go to the pipelined

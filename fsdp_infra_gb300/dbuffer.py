@@ -86,18 +86,22 @@ class DBuffer:
         return buf[o:o + rows * cols].view(rows, cols)
 
     def ptr_table(self, tensors: Sequence[torch.Tensor]) -> torch.Tensor:
-        """Device array of the tensors' data pointers (cached per pointer tuple)."""
+        """Device array of the tensors' data pointers, cached per tuple of
+        (pointer, element count, dtype): the checks run once per new tuple."""
         if len(tensors) != self.n:
             raise ValueError(f"expected {self.n} tensors, got {len(tensors)}")
-        for t, x in zip(range(self.n), tensors):
-            if not x.is_contiguous() or x.numel() != self.numel[t]:
-                raise ValueError(f"tensor {t} must be contiguous with {self.numel[t]} elements")
-            if x.device != self.device:
-                raise ValueError(f"tensor {t} is on {x.device}, expected {self.device}")
-        key = tuple(int(x.data_ptr()) for x in tensors)
+        key = tuple((x.data_ptr(), x.numel(), x.dtype) for x in tensors)
         tab = self._ptr_tables.get(key)
         if tab is None:
-            tab = torch.tensor(list(key) if key else [0], dtype=torch.int64, device=self.device)
+            for t, x in enumerate(tensors):
+                if x.dtype != tensors[0].dtype:
+                    raise TypeError("all tensors of one call must share one dtype")
+                if not x.is_contiguous() or x.numel() != self.numel[t]:
+                    raise ValueError(f"tensor {t} must be contiguous with {self.numel[t]} elements")
+                if x.device != self.device:
+                    raise ValueError(f"tensor {t} is on {x.device}, expected {self.device}")
+            ptrs = [k[0] for k in key] or [0]
+            tab = torch.tensor(ptrs, dtype=torch.int64, device=self.device)
             self._ptr_tables[key] = tab
         return tab
 
@@ -121,8 +125,6 @@ class DBuffer:
     def pack_cast(self, srcs: Sequence[torch.Tensor], buf: torch.Tensor, stream=None) -> None:
         self._check_buf(buf)
         sdt = dtype_code(srcs[0].dtype) if srcs else _c.DBUF_F32
-        if any(dtype_code(x.dtype) != sdt for x in srcs):
-            raise TypeError("all source tensors must share one dtype")
         tab = self.ptr_table(srcs)
         _c.dbuf_pack_cast(self.handle, tab.data_ptr(), sdt, buf.data_ptr(), dtype_code(buf.dtype),
                           self._stream(stream))
@@ -130,8 +132,6 @@ class DBuffer:
     def unpack(self, buf: torch.Tensor, dsts: Sequence[torch.Tensor], stream=None) -> None:
         self._check_buf(buf)
         ddt = dtype_code(dsts[0].dtype) if dsts else _c.DBUF_F32
-        if any(dtype_code(x.dtype) != ddt for x in dsts):
-            raise TypeError("all destination tensors must share one dtype")
         tab = self.ptr_table(dsts)
         _c.dbuf_unpack(self.handle, buf.data_ptr(), dtype_code(buf.dtype), tab.data_ptr(), ddt,
                        self._stream(stream))
