@@ -104,10 +104,23 @@ __device__ __forceinline__ float quot(float x, const Divisor &d) {
 
 template <int Q, bool EXACT>
 __device__ __forceinline__ uint32_t encode4(float4 v, const Divisor &d);
+// The reciprocal step on pairs with the packed fp32x2 multiply / fused
+// multiply-add of sm_100+: per element the same three IEEE operations as quot().
+__device__ __forceinline__ float2 quot2(float2 x, const Divisor &d) {
+    const float2 y2 = make_float2(d.y, d.y), ns2 = make_float2(-d.s, -d.s);
+    const float2 q = __fmul2_rn(x, y2);
+    const float2 r = __ffma2_rn(q, ns2, x);
+    return __ffma2_rn(r, y2, q);
+}
+
 template <>
 __device__ __forceinline__ uint32_t encode4<DBUF_QUANT_E4M3, false>(float4 v, const Divisor &d) {
-    const float2 lo = make_float2(quot<false>(v.x, d), quot<false>(v.y, d));
-    const float2 hi = make_float2(quot<false>(v.z, d), quot<false>(v.w, d));
+    float2 lo = quot2(make_float2(v.x, v.y), d);
+    float2 hi = quot2(make_float2(v.z, v.w), d);
+    lo.x = copysignf(lo.x, v.x);
+    lo.y = copysignf(lo.y, v.y);
+    hi.x = copysignf(hi.x, v.z);
+    hi.y = copysignf(hi.y, v.w);
     const uint32_t a = __nv_cvt_float2_to_fp8x2(lo, __NV_SATFINITE, __NV_E4M3);
     const uint32_t b = __nv_cvt_float2_to_fp8x2(hi, __NV_SATFINITE, __NV_E4M3);
     return (a & 0xFFFFu) | (b << 16);
@@ -129,15 +142,26 @@ __device__ __forceinline__ uint32_t encode4_int8(float4 v, const Divisor &d) {
 }
 template <>
 __device__ __forceinline__ uint32_t encode4<DBUF_QUANT_INT8, false>(float4 v, const Divisor &d) {
-    return encode4_int8<false>(v, d);
+    // the sign of a zero quotient does not change an INT8 code: no copysign
+    const float2 lo = quot2(make_float2(v.x, v.y), d);
+    const float2 hi = quot2(make_float2(v.z, v.w), d);
+    return encode1<DBUF_QUANT_INT8>(lo.x) | (encode1<DBUF_QUANT_INT8>(lo.y) << 8) |
+           (encode1<DBUF_QUANT_INT8>(hi.x) << 16) | (encode1<DBUF_QUANT_INT8>(hi.y) << 24);
 }
 template <>
 __device__ __forceinline__ uint32_t encode4<DBUF_QUANT_INT8, true>(float4 v, const Divisor &d) {
     return encode4_int8<true>(v, d);
 }
 
+// Three-input maximum (sm_100+); the inputs here are never NaN.
+__device__ __forceinline__ float max3f(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float abs_max4(float m, float4 v) {
-    return fmaxf(fmaxf(fmaxf(m, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
+    return max3f(max3f(m, fabsf(v.x), fabsf(v.y)), fabsf(v.z), fabsf(v.w));
 }
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -206,9 +230,10 @@ __device__ __forceinline__ void tile_body(const QItem &it, const TensorDesc &d,
         amax = warp_max(amax);
         if (lane == 0) sh_max[warp] = amax;
         __syncthreads();
-        amax = sh_max[0];
+        amax = sh_max[lane % kTileWarps];
 #pragma unroll
-        for (int i = 1; i < kTileWarps; ++i) amax = fmaxf(amax, sh_max[i]);
+        for (int o = kTileWarps / 2; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         scale = block_scale(amax, QParams<Q>::qmax);
         const Divisor dv = make_divisor(scale);
         if (!dv.exact) {
@@ -562,9 +587,10 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                      stages + s * kPipeStageBytes, &bars[s]);
             ++issued;
         }
-        amax = sh_max[(k & 1) * kPipeWarps];
+        amax = sh_max[(k & 1) * kPipeWarps + (lane % kPipeWarps)];
 #pragma unroll
-        for (int w = 1; w < kPipeWarps; ++w) amax = fmaxf(amax, sh_max[(k & 1) * kPipeWarps + w]);
+        for (int o = kPipeWarps / 2; o > 0; o >>= 1)
+            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
         if (g.quant == DBUF_QUANT_E4M3) {
             const float scale = block_scale(amax, QParams<DBUF_QUANT_E4M3>::qmax);
             pipe_encode_store<DBUF_QUANT_E4M3>(g, v, make_divisor(scale), warp, lane);
