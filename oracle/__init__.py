@@ -77,6 +77,11 @@ def lib():
         L.orc_block_quant.restype = i64
         L.orc_scale_offsets.argtypes = [i32, P, P, P, P, P, P]
         L.orc_scale_offsets.restype = i64
+        f = ctypes.c_float
+        L.orc_clip_coef.argtypes = [f, f]
+        L.orc_clip_coef.restype = f
+        L.orc_adamw.argtypes = [i32, P, P, P, P, P, P, f, f, f, f, f, f, f, f, f, i32]
+        L.orc_adamw.restype = None
         _lib = L
     return _lib
 
@@ -225,3 +230,23 @@ def block_quant(p: Plan, specs, buf: np.ndarray, codes: np.ndarray):
                                 _p(buf), _p(codes), _p(scales))
     assert got == total
     return scales[:total].copy()
+
+
+# ----------------------------------------------------------------------------
+# fused group optimizer step
+# ----------------------------------------------------------------------------
+
+def clip_coef(max_norm: float, total_norm: float) -> float:
+    return float(lib().orc_clip_coef(max_norm, total_norm))
+
+
+def adamw(p: Plan, params: np.ndarray, grad: np.ndarray, m: np.ndarray, v: np.ndarray, *,
+          lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
+          bc1: float, bc2: float, max_norm: float = 0.0, total_norm: float = 0.0,
+          nonfinite: int = 0) -> None:
+    """One AdamW step over the tensor ranges (in place on params, m, v)."""
+    for a in (params, grad, m, v):
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    lib().orc_adamw(len(p.offsets), _p(p.offsets), _p(_i64(p.numel)), _p(params), _p(grad),
+                    _p(m), _p(v), lr, beta1, beta2, eps, weight_decay, bc1, bc2, max_norm,
+                    total_norm, int(nonfinite))

@@ -417,3 +417,63 @@ int64_t orc_scale_offsets(int32_t n, const int64_t *rows, const int64_t *cols,
     }
     return s;
 }
+
+/* ------------------------------------------------------------------------ */
+/* Fused group optimizer step: AdamW over the flat buffer                    */
+/* ------------------------------------------------------------------------ */
+
+/* The scalars every element uses, each one fp32 operation in a fixed order. */
+typedef struct {
+    float coef;      /* gradient clip coefficient (1 when not clipping) */
+    float decay;     /* 1 - lr*wd */
+    float step;      /* lr / (1 - beta1^t) */
+    float omb1;      /* 1 - beta1 */
+    float omb2;      /* 1 - beta2 */
+} orc_adamw_scalars;
+
+/* Clip coefficient min(1, max_norm / (total_norm + 1e-6)) of gradient-norm
+ * clipping; no clipping when max_norm <= 0. */
+float orc_clip_coef(float max_norm, float total_norm)
+{
+    if (!(max_norm > 0.0f)) return 1.0f;
+    float denom = total_norm + 1e-6f;
+    float c = max_norm / denom;
+    return c < 1.0f ? c : 1.0f;
+}
+
+/* One AdamW step with decoupled weight decay over every tensor range of the
+ * flat buffer [veScale-3, OpDispatcher: fused AdamW handler on the local shard;
+ * veScale-FSDP, §5 DBuffer group-level operators].  The pages name the fused
+ * optimizer but not its formula; this is the standard AdamW update, every
+ * operation rounded to fp32 in this order:
+ *   g = grad * coef;  p = p * (1 - lr*wd)
+ *   m = beta1*m + (1-beta1)*g;  v = beta2*v + ((1-beta2)*g)*g
+ *   p = p - (lr/bc1) * (m / (sqrt(v / bc2) + eps))
+ * with bc1 = 1 - beta1^t and bc2 = 1 - beta2^t given by the caller.  When
+ * `nonfinite` is non-zero the step is skipped (nothing is written), as a
+ * gradient scaler skips a step with inf/NaN gradients. */
+void orc_adamw(int32_t n, const int64_t *offsets, const int64_t *numel, float *p,
+               const float *grad, float *m, float *v, float lr, float beta1, float beta2,
+               float eps, float wd, float bc1, float bc2, float max_norm, float total_norm,
+               int32_t nonfinite)
+{
+    if (nonfinite) return;
+    orc_adamw_scalars s;
+    s.coef = orc_clip_coef(max_norm, total_norm);
+    s.decay = 1.0f - lr * wd;
+    s.step = lr / bc1;
+    s.omb1 = 1.0f - beta1;
+    s.omb2 = 1.0f - beta2;
+    for (int32_t t = 0; t < n; ++t)
+        for (int64_t i = 0; i < numel[t]; ++i) {
+            int64_t j = offsets[t] + i;
+            float g = grad[j] * s.coef;
+            float pj = p[j] * s.decay;
+            float mj = beta1 * m[j] + s.omb1 * g;
+            float vj = beta2 * v[j] + (s.omb2 * g) * g;
+            float denom = sqrtf(vj / bc2) + eps;
+            p[j] = pj - s.step * (mj / denom);
+            m[j] = mj;
+            v[j] = vj;
+        }
+}
