@@ -522,6 +522,9 @@ def run_ours(args):
                 "bytes_per_launch": layer_bytes,
                 "traffic": _traffic_for(dom)}
 
+    # ---- the next row: fused AdamW step over every DBuffer (separate timing)
+    adamw = None if args.no_adamw else run_adamw(stack, args, world, peak, barrier)
+
     # ---- end to end: host inputs (pinned) -> device, operators, results -> host
     e2e = None if args.no_e2e else run_e2e(stack, args, world)
 
@@ -544,6 +547,7 @@ def run_ours(args):
                 "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": stack.launches_per_step * args.steps,
+                "next_rows": {"adamw": adamw} if adamw else None,
                 "launch": "eager" if args.eager else "cuda_graph (K steps captured once, replayed)",
                 "ops_note": ("per-operator times from one step with events around every "
                              "operator, outside the timed region" +
@@ -554,6 +558,62 @@ def run_ours(args):
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def run_adamw(stack, args, world, peak, barrier):
+    """The fused AdamW step (dbuf_adamw_step) over every DBuffer of the workload:
+    fp32 master parameters, the accumulated gradients and both moments in the
+    plan's layout, clipped to max_norm 1.0 with each DBuffer's own device norm and
+    non-finite flag from the step.  K steps captured once as a CUDA graph and
+    timed as one replay; 28 algorithmic bytes per element (read p, g, m, v; write
+    p, m, v)."""
+    device = stack.device
+    for d in stack.dbufs:
+        k = d["kind"]
+        if "p32" not in k:
+            k["p32"] = torch.zeros_like(k["acc"])
+            k["m32"] = torch.zeros_like(k["acc"])
+            k["v32"] = torch.zeros_like(k["acc"])
+            db = k["db"]
+            for t, x in enumerate(d["params"]):
+                k["p32"][db.offsets[t]:db.offsets[t] + x.numel()].copy_(x.reshape(-1))
+
+    def step(i):
+        for d in stack.dbufs:
+            k = d["kind"]
+            k["db"].adamw_step(k["p32"], k["acc"], k["m32"], k["v32"], step=i, lr=1e-4,
+                               betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1, max_norm=1.0,
+                               total_norm=d["out"][1], nonfinite=d["out"][2])
+
+    for i in range(1, max(args.warmup, 1) + 1):
+        step(i)
+    torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                step(10 + i)
+        graph.replay()
+        torch.cuda.synchronize()
+    barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(10 + i)
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e), device) / args.steps
+    nbytes = 28 * stack.elements
+    gbs = job_throughput(nbytes, ms, world)
+    return {"op": "dbuf_adamw_step (fp32 params/grads/moments, clip to the step's device norm)",
+            "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),
+            "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
+            "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 28,
+            "launches_per_step": len(stack.dbufs)}
 
 
 def run_e2e(stack, args, world):
@@ -661,6 +721,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of as one CUDA graph")
     ap.add_argument("--workload", default="dense7b",

@@ -187,3 +187,15 @@ extern "C" int dbuf_device_status(const dbuf_plan_t *p, int32_t *status, void *s
     *status = v;
     return DBUF_OK;
 }
+
+extern "C" int dbuf_adamw_step(const dbuf_plan_t *p, float *params, const float *grads,
+                               float *exp_avg, float *exp_avg_sq, const dbuf_adamw_hparams *hp,
+                               const float *total_norm, const int32_t *nonfinite, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!hp || !(hp->bias_correction1 > 0.0f) || !(hp->bias_correction2 > 0.0f))
+        return DBUF_EINVAL;
+    if (p->n > 0 && (!params || !grads || !exp_avg || !exp_avg_sq)) return DBUF_EINVAL;
+    return finish(dbuf::launch_adamw(p, params, grads, exp_avg, exp_avg_sq, *hp, total_norm,
+                                     nonfinite, stream));
+}

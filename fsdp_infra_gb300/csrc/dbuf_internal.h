@@ -103,6 +103,10 @@ int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_nor
 int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *scales,
                  void *stream);
 
+int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
+                 float *exp_avg_sq, const dbuf_adamw_hparams &hp, const float *total_norm,
+                 const int32_t *nonfinite, void *stream);
+
 size_t norm_workspace_bytes(const dbuf_plan_t *p);
 
 // One-time per-device set-up of the quantisation kernels (shared memory

@@ -35,6 +35,7 @@ DBUF_OP_UNPACK = 1
 DBUF_OP_SCALE_ACCUM_ZERO = 2
 DBUF_OP_NORM_NONFINITE = 3
 DBUF_OP_BLOCK_QUANT = 4
+DBUF_OP_ADAMW = 5
 
 _QUANT = {None: DBUF_QUANT_NONE, "none": DBUF_QUANT_NONE, "e4m3": DBUF_QUANT_E4M3,
           "int8": DBUF_QUANT_INT8}
@@ -43,7 +44,7 @@ _QUANT = {None: DBUF_QUANT_NONE, "none": DBUF_QUANT_NONE, "e4m3": DBUF_QUANT_E4M
 EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
-           "dbuf_device_status", "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_device_status", "dbuf_adamw_step", "dbuf_strerror", "dbuf_last_cuda_error")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -56,6 +57,12 @@ class DbufError(RuntimeError):
         if code == DBUF_ECUDA:
             msg += f", cudaError {_lib_handle().dbuf_last_cuda_error()}"
         super().__init__(msg)
+
+
+class dbuf_adamw_hparams(ctypes.Structure):
+    _fields_ = [(name, ctypes.c_float) for name in
+                ("lr", "beta1", "beta2", "eps", "weight_decay", "bias_correction1",
+                 "bias_correction2", "max_norm")]
 
 
 class dbuf_tensor_spec(ctypes.Structure):
@@ -103,6 +110,8 @@ def _lib_handle():
         L.dbuf_norm_nonfinite_noalloc.restype = ctypes.c_int
         L.dbuf_block_quant.argtypes = [P, P, P, P, P]
         L.dbuf_block_quant.restype = ctypes.c_int
+        L.dbuf_adamw_step.argtypes = [P, P, P, P, P, P, P, P, P]
+        L.dbuf_adamw_step.restype = ctypes.c_int
         L.dbuf_device_status.argtypes = [P, P, P]
         L.dbuf_device_status.restype = ctypes.c_int
         L.dbuf_strerror.argtypes = [ctypes.c_int]
@@ -208,6 +217,19 @@ def dbuf_norm_nonfinite_noalloc(plan: int, buf: int, dtype: int, tensor_norms: i
 
 def dbuf_block_quant(plan: int, buf: int, codes: int, scales: int, stream: int = 0) -> None:
     _check(_lib_handle().dbuf_block_quant(plan, buf, codes, scales, stream), "dbuf_block_quant")
+
+
+def dbuf_adamw_step(plan: int, params: int, grads: int, exp_avg: int, exp_avg_sq: int, *,
+                    lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
+                    bias_correction1: float, bias_correction2: float, max_norm: float = 0.0,
+                    total_norm: int = 0, nonfinite: int = 0, stream: int = 0) -> None:
+    """One AdamW step over the tensor ranges; total_norm / nonfinite are optional
+    device pointers (0 = not given)."""
+    hp = dbuf_adamw_hparams(lr, beta1, beta2, eps, weight_decay, bias_correction1,
+                            bias_correction2, max_norm)
+    _check(_lib_handle().dbuf_adamw_step(plan, params, grads, exp_avg, exp_avg_sq,
+                                         ctypes.byref(hp), total_norm or None, nonfinite or None,
+                                         stream), "dbuf_adamw_step")
 
 
 def dbuf_device_status(plan: int, stream: int = 0) -> int:

@@ -76,6 +76,7 @@ extern "C" {
 #define DBUF_OP_SCALE_ACCUM_ZERO 2
 #define DBUF_OP_NORM_NONFINITE 3
 #define DBUF_OP_BLOCK_QUANT 4
+#define DBUF_OP_ADAMW 5
 
 /*
  * One tensor of the group: a row-major [rows, cols] tensor (a 1-D vector is
@@ -290,6 +291,41 @@ int dbuf_norm_nonfinite_noalloc(const dbuf_plan_t *plan, const void *buf, int32_
  * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
  */
 int dbuf_device_status(const dbuf_plan_t *plan, int32_t *status, void *stream);
+
+/* Hyperparameters of one AdamW step (host struct, copied by value). */
+typedef struct dbuf_adamw_hparams {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;     /* decoupled: p *= 1 - lr*weight_decay */
+    float bias_correction1; /* 1 - beta1^t for step t >= 1, computed by the caller */
+    float bias_correction2; /* 1 - beta2^t */
+    float max_norm;         /* > 0: clip the gradient to this global L2 norm */
+} dbuf_adamw_hparams;
+
+/*
+ * dbuf_adamw_step -- fused group optimizer step: AdamW over every tensor range
+ * of fp32 buffers with the plan's layout, one launch.  [veScale OpDispatcher:
+ * fused AdamW/SGD handler on the local shard; veScale-FSDP §5 DBuffer
+ * group-level operators.]  The pages name the fused optimizer but not its
+ * formula; this is the standard decoupled-weight-decay AdamW, every operation
+ * rounded to fp32 in this order:
+ *   g = grad * coef;  p = p * (1 - lr*wd)
+ *   m = beta1*m + (1-beta1)*g;  v = beta2*v + ((1-beta2)*g)*g
+ *   p = p - (lr/bc1) * (m / (sqrt(v / bc2) + eps))
+ * coef = min(1, max_norm / (*total_norm + 1e-6)) when max_norm > 0 and
+ * total_norm is given (a device float, e.g. the output of dbuf_norm_nonfinite
+ * for the same gradients), else 1.  When nonfinite (a device int32, e.g. the
+ * flag of dbuf_norm_nonfinite) is given and non-zero, the step is skipped and
+ * nothing is written.  params, exp_avg, exp_avg_sq: device fp32 buffers,
+ * updated in place; grads: device fp32 buffer (e.g. the accumulator).  Padding
+ * is untouched.  Errors: DBUF_EINVAL (null pointers, non-positive bias
+ * corrections), DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_adamw_step(const dbuf_plan_t *plan, float *params, const float *grads, float *exp_avg,
+                    float *exp_avg_sq, const dbuf_adamw_hparams *hp, const float *total_norm,
+                    const int32_t *nonfinite, void *stream);
 
 /* dbuf_strerror -- static description of a return code. */
 const char *dbuf_strerror(int code);
