@@ -325,18 +325,41 @@ def oracle_sample_pass(reps=1):
     dst = np.zeros(n, np.uint16)
     codes = np.zeros(p.total, np.uint8)
     _, ns = oracle.scale_offsets([spec])
-    nbytes = (6 + 4 + 16 + 4 + 5) * n + 4 * ns
+    op_bytes = {"pack_cast": 6 * n, "unpack": 4 * n, "scale_accum_zero": 16 * n,
+                "norm_nonfinite": 4 * n, "block_quant": 5 * n + 4 * ns}
+    nbytes = sum(op_bytes.values())
+    op_time = dict.fromkeys(op_bytes, 0.0)
     t0 = time.perf_counter()
     for _ in range(reps):
-        oracle.pack(p, [src], b16)
-        oracle.unpack(p, b16, [dst])
-        oracle.scale_accum_zero(p, grad, acc, w.scale)
-        oracle.norm_nonfinite(p, acc)
-        oracle.block_quant(p, [spec], acc, codes)
+        for op, fn in (("pack_cast", lambda: oracle.pack(p, [src], b16)),
+                       ("unpack", lambda: oracle.unpack(p, b16, [dst])),
+                       ("scale_accum_zero", lambda: oracle.scale_accum_zero(p, grad, acc, w.scale)),
+                       ("norm_nonfinite", lambda: oracle.norm_nonfinite(p, acc)),
+                       ("block_quant", lambda: oracle.block_quant(p, [spec], acc, codes))):
+            t1 = time.perf_counter()
+            fn()
+            op_time[op] += time.perf_counter() - t1
     dt = time.perf_counter() - t0
     desc = (f"{REF_SAMPLE_ROWS}x{emb.cols} slice of the embedding table as one DBuffer "
             f"(m={w.m}, {n} elements), all five operators, x{reps}")
+    oracle_sample_pass.last_ops = {op: round(op_bytes[op] * reps / op_time[op] / 1e9, 4)
+                                   for op in op_bytes}
     return nbytes * reps / dt / 1e9, n * reps / dt, dt, desc
+
+
+def _host_cpu():
+    """Core count and CPU model of this host (the oracle runs on one core)."""
+    model = None
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+    except OSError:
+        pass
+    import platform
+    return {"nproc": os.cpu_count(), "machine": platform.machine(), "model": model}
 
 
 def run_reference(args):
@@ -360,7 +383,9 @@ def run_reference(args):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": _config_dict(None, "dense7b"),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
-                             "kind": "oracle", "sample": desc},
+                             "kind": "oracle", "sample": desc,
+                             "ops_gbs": getattr(oracle_sample_pass, "last_ops", None),
+                             "host": _host_cpu()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -536,7 +561,9 @@ def run_ours(args):
             oracle.build()
             gbs, eps, dt, desc = oracle_sample_pass(1)
             cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                   "sample": desc, "seconds": round(dt, 2)}
+                   "sample": desc, "seconds": round(dt, 2),
+                   "ops_gbs": getattr(oracle_sample_pass, "last_ops", None),
+                   "host": _host_cpu()}
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
                 "steps": args.steps, "warmup": args.warmup,
                 "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
