@@ -82,6 +82,13 @@ def lib():
         L.orc_clip_coef.restype = f
         L.orc_adamw.argtypes = [i32, P, P, P, P, P, P, f, f, f, f, f, f, f, f, f, i32]
         L.orc_adamw.restype = None
+        L.orc_v_code.argtypes = [f, f]
+        L.orc_v_code.restype = ctypes.c_uint8
+        L.orc_state_offsets.argtypes = [i32, P, P, P]
+        L.orc_state_offsets.restype = ctypes.c_int64
+        L.orc_adamw8.argtypes = [i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
+                                 f, f, f, f, f, f, f, f, f, i32]
+        L.orc_adamw8.restype = None
         _lib = L
     return _lib
 
@@ -250,3 +257,45 @@ def adamw(p: Plan, params: np.ndarray, grad: np.ndarray, m: np.ndarray, v: np.nd
     lib().orc_adamw(len(p.offsets), _p(p.offsets), _p(_i64(p.numel)), _p(params), _p(grad),
                     _p(m), _p(v), lr, beta1, beta2, eps, weight_decay, bc1, bc2, max_norm,
                     total_norm, int(nonfinite))
+
+
+
+def v_code(v: float, scale: float) -> int:
+    """The second moment's 8-bit code: nearest level (c + 1) * scale."""
+    return int(lib().orc_v_code(float(v), float(scale)))
+
+
+def state_offsets(specs):
+    """(state_offsets[n], n_state): where each unquantised tensor's fp32 moments
+    start in the compact 8-bit-AdamW state (-1 for quantised tensors)."""
+    n = len(specs)
+    numel = _i64([s.numel for s in specs])
+    q = _i32([_QUANT[s.quant] for s in specs])
+    out = np.zeros(max(n, 1), np.int64)
+    total = lib().orc_state_offsets(n, _p(numel), _p(q), _p(out))
+    return out[:n].copy(), int(total)
+
+
+def adamw8(p: Plan, specs, params: np.ndarray, grad: np.ndarray, m_codes: np.ndarray,
+           v_codes: np.ndarray, m_scales: np.ndarray, v_scales: np.ndarray, m32: np.ndarray,
+           v32: np.ndarray, *, lr: float, beta1: float, beta2: float, eps: float,
+           weight_decay: float, bc1: float, bc2: float, max_norm: float = 0.0,
+           total_norm: float = 0.0, nonfinite: int = 0) -> None:
+    """One 8-bit AdamW step (in place): INT8 block moments (codes in the flat
+    buffer's layout, one fp32 scale per block) for quantised tensors, compact
+    fp32 moments (m32, v32 at state_offsets) for the rest."""
+    n = len(specs)
+    r = _i64([s.rows for s in specs]); c = _i64([s.cols for s in specs])
+    qr = _i64([s.qblock[0] for s in specs]); qc = _i64([s.qblock[1] for s in specs])
+    q = _i32([_QUANT[s.quant] for s in specs])
+    so, n_state = state_offsets(specs)
+    so = np.ascontiguousarray(so if n else np.zeros(1, np.int64))
+    for a in (params, grad, m_scales, v_scales, m32, v32):
+        assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
+    assert m_codes.dtype == np.uint8 and v_codes.dtype == np.uint8
+    assert m32.size >= n_state and v32.size >= n_state
+    assert m_codes.size >= p.total and v_codes.size >= p.total and params.size >= p.total
+    lib().orc_adamw8(n, _p(p.offsets), _p(r), _p(c), _p(qr), _p(qc), _p(q), _p(so), _p(params),
+                     _p(grad), _p(m_codes), _p(v_codes), _p(m_scales), _p(v_scales), _p(m32),
+                     _p(v32), lr, beta1, beta2, eps, weight_decay, bc1, bc2, max_norm,
+                     total_norm, int(nonfinite))

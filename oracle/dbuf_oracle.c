@@ -477,3 +477,126 @@ void orc_adamw(int32_t n, const int64_t *offsets, const int64_t *numel, float *p
             v[j] = vj;
         }
 }
+
+/* Layout of the fp32 moments that 8-bit AdamW keeps for tensors without a
+ * quantisation block (vectors, norms): those tensors in group order, each
+ * starting at a multiple of 4 elements (16 bytes); -1 for quantised tensors.
+ * Returns the number of fp32 elements per moment. */
+int64_t orc_state_offsets(int32_t n, const int64_t *numel, const int32_t *quant,
+                          int64_t *state_offsets)
+{
+    int64_t s = 0;
+    for (int32_t t = 0; t < n; ++t) {
+        if (quant[t] != ORC_QNONE) { state_offsets[t] = -1; continue; }
+        state_offsets[t] = s;
+        s += (numel[t] + 3) / 4 * 4;
+    }
+    return s;
+}
+
+/* The second moment's 8-bit code (unsigned): the linear absmax map without a
+ * zero level, code c stands for (c + 1) * scale with scale = block amax / 256,
+ * so a positive v never dequantises to 0 (a zero denominator would turn the
+ * update into m / eps).  c = clamp(rint(v / scale), 1, 256) - 1 with v / scale
+ * one fp32 division; an all-zero block has scale 0 and codes 0. */
+uint8_t orc_v_code(float v, float scale)
+{
+    if (!(scale > 0.0f) || isnan(v)) return 0;
+    float r = rintf(v / scale);
+    if (r < 1.0f) r = 1.0f;
+    if (r > 256.0f) r = 256.0f;
+    return (uint8_t)((int)r - 1);
+}
+
+/* 8-bit AdamW: the same step with block-wise 8-bit moments [veScale-FSDP, §6.3
+ * 8-bit Adam: block-wise INT8 quantisation of the optimizer's gradient
+ * statistics; blocks never cross a shard, so each shard quantises locally].
+ * The pages do not give the code maps.  Reading: the first moment m takes the
+ * signed absmax INT8 map of orc_block_quant (scale = amax / 127, 1 when not
+ * positive; code = clamp(rint(m / scale), -127, 127); m = code * scale); the
+ * second moment v >= 0 takes orc_v_code's zero-free unsigned map (v = (c + 1) *
+ * scale).  Per block of each quantised tensor's quantisation shape: dequantise
+ * (one fp32 multiply each), the AdamW step of orc_adamw, new block scales from
+ * the new moments' amax, re-encode.  The codes share the flat buffer's layout;
+ * scales are indexed like orc_block_quant's.  Tensors with quant = none keep
+ * fp32 moments in m32 / v32 at their state offset (orc_state_offsets).  A set
+ * non-finite flag skips the step. */
+void orc_adamw8(int32_t n, const int64_t *offsets, const int64_t *rows, const int64_t *cols,
+                const int64_t *qrows, const int64_t *qcols, const int32_t *quant,
+                const int64_t *state_offsets, float *p, const float *grad, uint8_t *m_codes,
+                uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
+                float lr, float beta1, float beta2, float eps, float wd, float bc1, float bc2,
+                float max_norm, float total_norm, int32_t nonfinite)
+{
+    if (nonfinite) return;
+    orc_adamw_scalars s;
+    s.coef = orc_clip_coef(max_norm, total_norm);
+    s.decay = 1.0f - lr * wd;
+    s.step = lr / bc1;
+    s.omb1 = 1.0f - beta1;
+    s.omb2 = 1.0f - beta2;
+    int64_t s_off = 0;
+    for (int32_t t = 0; t < n; ++t) {
+        int64_t R = rows[t], C = cols[t];
+        if (quant[t] == ORC_QNONE) {
+            for (int64_t i = 0; i < R * C; ++i) {
+                int64_t j = offsets[t] + i, k = state_offsets[t] + i;
+                float g = grad[j] * s.coef;
+                float pj = p[j] * s.decay;
+                float mj = beta1 * m32[k] + s.omb1 * g;
+                float vj = beta2 * v32[k] + (s.omb2 * g) * g;
+                float denom = sqrtf(vj / bc2) + eps;
+                p[j] = pj - s.step * (mj / denom);
+                m32[k] = mj;
+                v32[k] = vj;
+            }
+            continue;
+        }
+        int64_t qr = qrows[t] > 0 ? qrows[t] : R;
+        int64_t qc = qcols[t] > 0 ? qcols[t] : C;
+        int64_t nbr = nblocks_dim(R, qr), nbc = nblocks_dim(C, qc);
+        for (int64_t bi = 0; bi < nbr; ++bi)
+            for (int64_t bj = 0; bj < nbc; ++bj) {
+                int64_t r0 = bi * qr, r1 = r0 + qr < R ? r0 + qr : R;
+                int64_t c0 = bj * qc, c1 = c0 + qc < C ? c0 + qc : C;
+                int64_t si = s_off + bi * nbc + bj;
+                float ms_old = m_scales[si], vs_old = v_scales[si];
+                float mamax = 0.0f, vamax = 0.0f;
+                /* pass 1: dequantise and step the moments to find the new block
+                 * amax (pass 2 repeats the identical operations) */
+                for (int64_t r = r0; r < r1; ++r)
+                    for (int64_t c = c0; c < c1; ++c) {
+                        int64_t j = offsets[t] + r * C + c;
+                        float mo = (float)(int8_t)m_codes[j] * ms_old;
+                        float vo = ((float)v_codes[j] + 1.0f) * vs_old;
+                        float g = grad[j] * s.coef;
+                        float mj = beta1 * mo + s.omb1 * g;
+                        float vj = beta2 * vo + (s.omb2 * g) * g;
+                        if (fabsf(mj) > mamax) mamax = fabsf(mj);
+                        if (fabsf(vj) > vamax) vamax = fabsf(vj);
+                    }
+                float ms_new = mamax / 127.0f;
+                if (!(ms_new > 0.0f)) ms_new = 1.0f;
+                float vs_new = vamax / 256.0f;
+                /* pass 2: the same step again (identical operations), update the
+                 * parameters, encode the new moments */
+                for (int64_t r = r0; r < r1; ++r)
+                    for (int64_t c = c0; c < c1; ++c) {
+                        int64_t j = offsets[t] + r * C + c;
+                        float mo = (float)(int8_t)m_codes[j] * ms_old;
+                        float vo = ((float)v_codes[j] + 1.0f) * vs_old;
+                        float g = grad[j] * s.coef;
+                        float pj = p[j] * s.decay;
+                        float mj = beta1 * mo + s.omb1 * g;
+                        float vj = beta2 * vo + (s.omb2 * g) * g;
+                        float denom = sqrtf(vj / bc2) + eps;
+                        p[j] = pj - s.step * (mj / denom);
+                        m_codes[j] = (uint8_t)orc_f32_to_int8(mj / ms_new);
+                        v_codes[j] = orc_v_code(vj, vs_new);
+                    }
+                m_scales[si] = ms_new;
+                v_scales[si] = vs_new;
+            }
+        s_off += nbr * nbc;
+    }
+}
