@@ -549,6 +549,7 @@ def run_ours(args):
 
     # ---- the next row: fused AdamW step over every DBuffer (separate timing)
     adamw = None if args.no_adamw else run_adamw(stack, args, world, peak, barrier)
+    adamw8 = None if args.no_adamw else run_adamw8(stack, args, world, peak, barrier)
 
     # ---- end to end: host inputs (pinned) -> device, operators, results -> host
     e2e = None if args.no_e2e else run_e2e(stack, args, world)
@@ -574,7 +575,7 @@ def run_ours(args):
                 "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": stack.launches_per_step * args.steps,
-                "next_rows": {"adamw": adamw} if adamw else None,
+                "next_rows": ({"adamw": adamw, "adamw8": adamw8} if adamw else None),
                 "launch": "eager" if args.eager else "cuda_graph (K steps captured once, replayed)",
                 "ops_note": ("per-operator times from one step with events around every "
                              "operator, outside the timed region" +
@@ -641,6 +642,81 @@ def run_adamw(stack, args, world, peak, barrier):
             "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
             "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 28,
             "launches_per_step": len(stack.dbufs)}
+
+
+def run_adamw8(stack, args, world, peak, barrier):
+    """8-bit AdamW (dbuf_adamw8_step) over every DBuffer of the workload, each
+    group re-planned as the 8-bit Adam experiment shards it (32x32 INT8 blocks,
+    32-row granularity for matrices): fp32 master parameters and gradients,
+    8-bit block moments, compact fp32 moments for vectors; clipped to max_norm
+    1.0 with the group's device norm.  One plan and one set of buffers per group
+    kind, stepped once per DBuffer (the buffers exceed L2).  K steps captured
+    once as a CUDA graph and timed as one replay.  Algorithmic bytes: 16 per
+    element of a quantised tensor (read p, g and two codes; write p and two
+    codes), 28 per element of the others, 16 per block (two scales read and
+    written)."""
+    from fsdp_infra_gb300 import DBuffer
+    from workloads import grad_values, param_values
+    from workloads.configs import adam8_group
+    device = stack.device
+    w = stack.w
+    kinds = {}
+    for gi, g in enumerate(w.groups):
+        g8 = adam8_group(g)
+        db = DBuffer(g8.tensors, w.m, None, w.align, device=device).upload()
+        p32 = torch.zeros(db.total, dtype=torch.float32, device=device)
+        g32 = torch.zeros(db.total, dtype=torch.float32, device=device)
+        for t, spec in enumerate(g8.tensors):
+            o = db.offsets[t]
+            p32[o:o + spec.numel].copy_(param_values(w, gi, t, device=device).reshape(-1))
+            g32[o:o + spec.numel].copy_(grad_values(w, gi, t, device=device).reshape(-1).float())
+        out = db.norm_nonfinite(g32)
+        qe = sum(spec.numel for spec in g8.tensors if spec.quant)
+        pe = sum(spec.numel for spec in g8.tensors if not spec.quant)
+        kinds[gi] = {"db": db, "p": p32, "g": g32, "state": db.new_adamw8_state(), "out": out,
+                     "bytes": 16 * qe + 28 * pe + 16 * db.n_scales}
+    order = [d["kind"]["gi"] for d in stack.dbufs]
+
+    def step(i):
+        for gi in order:
+            k = kinds[gi]
+            k["db"].adamw8_step(k["p"], k["g"], k["state"], step=i, lr=1e-4, betas=(0.9, 0.95),
+                                eps=1e-8, weight_decay=0.1, max_norm=1.0, total_norm=k["out"][1],
+                                nonfinite=k["out"][2])
+
+    for i in range(1, max(args.warmup, 1) + 1):
+        step(i)
+    torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(args.steps):
+                step(10 + i)
+        graph.replay()
+        torch.cuda.synchronize()
+    barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        for i in range(args.steps):
+            step(10 + i)
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e), device) / args.steps
+    nbytes = sum(kinds[gi]["bytes"] for gi in order)
+    gbs = job_throughput(nbytes, ms, world)
+    elems = sum(kinds[gi]["db"].total for gi in order)
+    blk = sorted({spec.qblock for g in w.groups for spec in adam8_group(g).tensors if spec.quant})
+    return {"op": "dbuf_adamw8_step (fp32 params/grads, 8-bit block moments, clip to the "
+                  "group's device norm)",
+            "blocks": [list(b) for b in blk], "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),
+            "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
+            "frac_of_peak": round(gbs / world / peak, 4),
+            "bytes_per_step": nbytes, "flat_elements_per_step": elems,
+            "launches_per_step": len(order)}
 
 
 def run_e2e(stack, args, world):

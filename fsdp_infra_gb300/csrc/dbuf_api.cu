@@ -50,7 +50,9 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     const size_t b_r = align256(sizeof(dbuf::RowItem) * p->row_items.size());
     const size_t b_q = align256(sizeof(dbuf::QItem) * p->tile_items.size());
     const size_t b_p = align256(sizeof(dbuf::TileItem) * p->pipe_items.size());
-    const size_t bytes = b_t + b_c + b_r + b_q + b_p + 256;
+    const size_t b_o = align256(sizeof(dbuf::OptItem) * p->opt_items.size());
+    const size_t b_a = align256(sizeof(int32_t) * p->opt_plain.size());
+    const size_t bytes = b_t + b_c + b_r + b_q + b_p + b_o + b_a + 256;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -72,7 +74,9 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     t.row_items = reinterpret_cast<dbuf::RowItem *>(c + b_t + b_c);
     t.tile_items = reinterpret_cast<dbuf::QItem *>(c + b_t + b_c + b_r);
     t.pipe_items = reinterpret_cast<dbuf::TileItem *>(c + b_t + b_c + b_r + b_q);
-    t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p);
+    t.opt_items = reinterpret_cast<dbuf::OptItem *>(c + b_t + b_c + b_r + b_q + b_p);
+    t.opt_plain = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o);
+    t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a);
     t.num_sms = sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = cudaMemsetAsync(t.status, 0, sizeof(int32_t), st);
@@ -84,12 +88,14 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
         void *dst;
         const void *src;
         size_t n;
-    } pieces[5] = {
+    } pieces[7] = {
         {t.tensors, p->tdesc.data(), sizeof(dbuf::TensorDesc) * p->tdesc.size()},
         {t.chunks, p->chunks.data(), sizeof(dbuf::Chunk) * p->chunks.size()},
         {t.row_items, p->row_items.data(), sizeof(dbuf::RowItem) * p->row_items.size()},
         {t.tile_items, p->tile_items.data(), sizeof(dbuf::QItem) * p->tile_items.size()},
         {t.pipe_items, p->pipe_items.data(), sizeof(dbuf::TileItem) * p->pipe_items.size()},
+        {t.opt_items, p->opt_items.data(), sizeof(dbuf::OptItem) * p->opt_items.size()},
+        {t.opt_plain, p->opt_plain.data(), sizeof(int32_t) * p->opt_plain.size()},
     };
     for (const Piece &pc : pieces) {
         if (!pc.n) continue;
@@ -198,4 +204,24 @@ extern "C" int dbuf_adamw_step(const dbuf_plan_t *p, float *params, const float 
     if (p->n > 0 && (!params || !grads || !exp_avg || !exp_avg_sq)) return DBUF_EINVAL;
     return finish(dbuf::launch_adamw(p, params, grads, exp_avg, exp_avg_sq, *hp, total_norm,
                                      nonfinite, stream));
+}
+
+extern "C" int dbuf_adamw8_step(const dbuf_plan_t *p, float *params, const float *grads,
+                                uint8_t *exp_avg_codes, uint8_t *exp_avg_sq_codes,
+                                float *exp_avg_scales, float *exp_avg_sq_scales,
+                                float *exp_avg_fp32, float *exp_avg_sq_fp32,
+                                const dbuf_adamw_hparams *hp, const float *total_norm,
+                                const int32_t *nonfinite, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!hp || !(hp->bias_correction1 > 0.0f) || !(hp->bias_correction2 > 0.0f))
+        return DBUF_EINVAL;
+    if (p->n > 0 && (!params || !grads)) return DBUF_EINVAL;
+    if (p->n_scales > 0 &&
+        (!exp_avg_codes || !exp_avg_sq_codes || !exp_avg_scales || !exp_avg_sq_scales))
+        return DBUF_EINVAL;
+    if (p->n_state > 0 && (!exp_avg_fp32 || !exp_avg_sq_fp32)) return DBUF_EINVAL;
+    return finish(dbuf::launch_adamw8(p, params, grads, exp_avg_codes, exp_avg_sq_codes,
+                                      exp_avg_scales, exp_avg_sq_scales, exp_avg_fp32,
+                                      exp_avg_sq_fp32, *hp, total_norm, nonfinite, stream));
 }

@@ -17,13 +17,14 @@ constexpr int64_t kChunkElems = 16384;
 // Blocks per work item of the row-block (1 x qc) quantisation kernel.
 constexpr int32_t kRowItemBlocks = 64;
 
-// One tensor of the group, as the kernels see it (64 bytes).
+// One tensor of the group, as the kernels see it (72 bytes).
 struct TensorDesc {
     int64_t buf_off;    // l_t
     int64_t numel;      // n_t
     int64_t rows;
     int64_t cols;
     int64_t scale_off;  // first block scale of this tensor
+    int64_t state_off;  // first fp32 moment in the compact 8-bit-optimizer state, or -1
     int32_t qrows;      // effective quantisation block rows (>= 1)
     int32_t qcols;      // effective quantisation block cols (>= 1)
     int32_t quant;      // DBUF_QUANT_*
@@ -31,7 +32,7 @@ struct TensorDesc {
     int32_t chunk_begin;
     int32_t chunk_end;
 };
-static_assert(sizeof(TensorDesc) == 64, "TensorDesc layout");
+static_assert(sizeof(TensorDesc) == 72, "TensorDesc layout");
 
 // A contiguous piece of one tensor: elements [off, off+len) of tensor `tensor`.
 struct Chunk {
@@ -73,6 +74,23 @@ struct TileItem {
 };
 static_assert(sizeof(TileItem) == 16, "TileItem layout");
 
+// A run of `count` consecutive quantisation blocks (row-major block order) of
+// one tensor for the 8-bit optimizer step, starting at block `first`; `lanes`
+// threads (4, 8, 16 or 32) work on one block.
+struct OptItem {
+    int64_t first;
+    int32_t tensor;
+    int16_t count;
+    int16_t lanes;
+};
+static_assert(sizeof(OptItem) == 16, "OptItem layout");
+
+// Moment units (4 elements on the vector path) that one lane of the 8-bit
+// optimizer keeps in registers; larger blocks are recomputed in a second pass.
+constexpr int kOptUnitsPerLane = 8;
+// Target elements per 8-bit optimizer work item.
+constexpr int64_t kOptItemElems = 16384;
+
 constexpr int kPipeMaxRows = 128;
 constexpr int kPipeMaxCols = 128;
 constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch
@@ -83,6 +101,8 @@ struct DeviceTables {
     RowItem *row_items = nullptr;    // blocks with qrows == 1
     QItem *tile_items = nullptr;     // other blocks with qrows > 1 (one block per item)
     TileItem *pipe_items = nullptr;  // tiles for the pipelined kernel
+    OptItem *opt_items = nullptr;    // 8-bit optimizer: blocks of quantised tensors
+    int32_t *opt_plain = nullptr;    // 8-bit optimizer: chunks of the other tensors
     int32_t *status = nullptr;       // device status word (0, or DBUF_ETIMEOUT)
     void *base = nullptr;
     size_t bytes = 0;
@@ -106,6 +126,11 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
 int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
                  float *exp_avg_sq, const dbuf_adamw_hparams &hp, const float *total_norm,
                  const int32_t *nonfinite, void *stream);
+
+int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8_t *m_codes,
+                  uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
+                  const dbuf_adamw_hparams &hp, const float *total_norm, const int32_t *nonfinite,
+                  void *stream);
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p);
 
@@ -139,6 +164,10 @@ struct dbuf_plan {
     std::vector<dbuf::QItem> tile_items;
     std::vector<dbuf::TileItem> pipe_items;
     std::vector<int32_t> pipe_tensors;  // slot -> tensor id
+    std::vector<dbuf::OptItem> opt_items;
+    std::vector<int32_t> opt_plain;      // chunk ids of tensors without quantisation
+    std::vector<int64_t> state_offsets;  // [n], -1 for quantised tensors
+    int64_t n_state = 0;
 
     bool uploaded = false;
     dbuf::DeviceTables dev;

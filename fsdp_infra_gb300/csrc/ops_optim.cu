@@ -13,7 +13,21 @@
 // non-finite flag skips the whole step, as a gradient scaler skips a step with
 // inf/NaN gradients.  Tensor ranges only; 28 bytes per element (read p, g, m,
 // v; write p, m, v).
-#include "common.cuh"
+//
+// 8-bit AdamW (§6.3 8-bit Adam: block-wise INT8 quantisation of the gradient
+// statistics, blocks inside shards) runs the same step on block-quantised
+// moments: per quantisation block of a tensor, m = code * scale (signed INT8,
+// scale = amax / 127) and v = (code + 1) * scale (unsigned 8-bit without a zero
+// level, scale = amax / 256); the fp32 step; new block scales from the new
+// moments' amax; re-encoding with the correctly rounded quotient of
+// quant_math.cuh.  A group of 4..32 lanes owns one block: pass 1 loads the
+// gradients and codes, keeps the new moments in registers and reduces the block
+// maxima with shuffles; pass 2 loads the parameters, updates them and writes
+// the codes (blocks with more than lanes * kOptUnitsPerLane units recompute the
+// moments in pass 2 instead).  Unquantised tensors keep compact fp32 moments and
+// take the fp32 path in the same launch.  16 bytes per element (read p, g and
+// two codes; write p and two codes) plus 16 bytes per block.
+#include "quant_math.cuh"
 
 namespace dbuf {
 namespace {
@@ -43,31 +57,34 @@ __device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp
     return s;
 }
 
-__device__ __forceinline__ void adam_elem(const AdamScalars &s, float &p, float g, float &m,
-                                          float &v) {
+// The moments' update (m, v in and out).
+__device__ __forceinline__ void adam_moments(const AdamScalars &s, float g, float &m, float &v) {
     g = __fmul_rn(g, s.coef);
-    const float pd = __fmul_rn(p, s.decay);
     m = __fadd_rn(__fmul_rn(s.beta1, m), __fmul_rn(s.omb1, g));
     v = __fadd_rn(__fmul_rn(s.beta2, v), __fmul_rn(__fmul_rn(s.omb2, g), g));
-    const float denom = __fadd_rn(__fsqrt_rn(__fdiv_rn(v, s.bc2)), s.eps);
-    p = __fsub_rn(pd, __fmul_rn(s.step, __fdiv_rn(m, denom)));
 }
 
-__global__ void __launch_bounds__(kThreads)
-    adamw_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
-                 float *__restrict__ params, const float *__restrict__ grads,
-                 float *__restrict__ exp_avg, float *__restrict__ exp_avg_sq,
-                 const dbuf_adamw_hparams hp, const float *__restrict__ total_norm,
-                 const int32_t *__restrict__ nonfinite) {
-    if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
-    const AdamScalars s = adam_scalars(hp, total_norm);
-    const Chunk c = chunks[blockIdx.x];
-    const int64_t base = td[c.tensor].buf_off + c.off;
-    char *p = reinterpret_cast<char *>(params + base);
-    const char *g = reinterpret_cast<const char *>(grads + base);
-    char *m = reinterpret_cast<char *>(exp_avg + base);
-    char *v = reinterpret_cast<char *>(exp_avg_sq + base);
-    const int len = c.len;
+// The parameter's update from the new moments.
+__device__ __forceinline__ float adam_param(const AdamScalars &s, float p, float m, float v) {
+    const float pd = __fmul_rn(p, s.decay);
+    const float denom = __fadd_rn(__fsqrt_rn(__fdiv_rn(v, s.bc2)), s.eps);
+    return __fsub_rn(pd, __fmul_rn(s.step, __fdiv_rn(m, denom)));
+}
+
+__device__ __forceinline__ void adam_elem(const AdamScalars &s, float &p, float g, float &m,
+                                          float &v) {
+    adam_moments(s, g, m, v);
+    p = adam_param(s, p, m, v);
+}
+
+// AdamW over `len` elements of fp32 parameters, gradients and moments.
+__device__ __forceinline__ void adamw_range(const AdamScalars &s, float *params,
+                                            const float *grads, float *exp_avg,
+                                            float *exp_avg_sq, int len) {
+    char *p = reinterpret_cast<char *>(params);
+    const char *g = reinterpret_cast<const char *>(grads);
+    char *m = reinterpret_cast<char *>(exp_avg);
+    char *v = reinterpret_cast<char *>(exp_avg_sq);
     const bool vec = aligned16(p, g) && aligned16(m, v);
     const int nv = vec ? len / kVec : 0;
     for (int b0 = 0; b0 < nv; b0 += kThreads * kUnroll) {
@@ -112,6 +129,256 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+__global__ void __launch_bounds__(kThreads)
+    adamw_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
+                 float *__restrict__ params, const float *__restrict__ grads,
+                 float *__restrict__ exp_avg, float *__restrict__ exp_avg_sq,
+                 const dbuf_adamw_hparams hp, const float *__restrict__ total_norm,
+                 const int32_t *__restrict__ nonfinite) {
+    if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
+    const AdamScalars s = adam_scalars(hp, total_norm);
+    const Chunk c = chunks[blockIdx.x];
+    const int64_t base = td[c.tensor].buf_off + c.off;
+    adamw_range(s, params + base, grads + base, exp_avg + base, exp_avg_sq + base, c.len);
+}
+
+// ---------------------------------------------------------------------------
+// 8-bit AdamW
+// ---------------------------------------------------------------------------
+
+// A lane's unit is W consecutive elements of one block row (W = 4 on the
+// vector path).  STREAM marks loads of data read once (evict-first).
+template <int W, bool STREAM>
+__device__ __forceinline__ void load_f(const float *p, int64_t e, float (&x)[W]) {
+    if constexpr (W == 4) {
+        const float4 *a = reinterpret_cast<const float4 *>(p + e);
+        const float4 t = STREAM ? __ldcs(a) : *a;
+        x[0] = t.x; x[1] = t.y; x[2] = t.z; x[3] = t.w;
+    } else {
+        x[0] = STREAM ? __ldcs(p + e) : p[e];
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void store_f(float *p, int64_t e, const float (&x)[W]) {
+    if constexpr (W == 4)
+        __stcs(reinterpret_cast<float4 *>(p + e), make_float4(x[0], x[1], x[2], x[3]));
+    else
+        __stcs(p + e, x[0]);
+}
+
+template <int W, bool STREAM>
+__device__ __forceinline__ uint32_t load_c(const uint8_t *c, int64_t e) {
+    if constexpr (W == 4) {
+        const unsigned int *a = reinterpret_cast<const unsigned int *>(c + e);
+        return STREAM ? __ldcs(a) : *a;
+    } else {
+        return c[e];
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void store_c(uint8_t *c, int64_t e, uint32_t x) {
+    if constexpr (W == 4)
+        __stcs(reinterpret_cast<unsigned int *>(c + e), x);
+    else
+        c[e] = uint8_t(x);
+}
+
+// Dequantise a unit's codes and step its moments; updates the block maxima.
+template <int W, bool STREAM>
+__device__ __forceinline__ void unit_moments(const AdamScalars &s, const float *grads,
+                                             const uint8_t *mc, const uint8_t *vc, int64_t e,
+                                             float ms_old, float vs_old, float (&m)[W],
+                                             float (&v)[W], float &mamax, float &vamax) {
+    float g[W];
+    load_f<W, STREAM>(grads, e, g);
+    const uint32_t cm = load_c<W, STREAM>(mc, e), cv = load_c<W, STREAM>(vc, e);
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        m[w] = __fmul_rn(__int2float_rn(int(int8_t(uint8_t(cm >> (8 * w))))), ms_old);
+        v[w] = __fmul_rn(__int2float_rn(int((cv >> (8 * w)) & 0xFFu) + 1), vs_old);
+        adam_moments(s, g[w], m[w], v[w]);
+        mamax = fmaxf(mamax, fabsf(m[w]));
+        vamax = fmaxf(vamax, v[w]);
+    }
+}
+
+// The second moment's code: nearest level (c + 1) * scale, c in [0, 255].
+template <bool EXACT>
+__device__ __forceinline__ uint32_t v_code(float v, const Divisor &d) {
+    const int c = __float2int_rn(quot<EXACT>(v, d));
+    return uint32_t(min(256, max(1, c)) - 1);
+}
+
+// Pass 2 of one unit: parameters, then both codes.
+template <int W, bool EXACT>
+__device__ __forceinline__ void unit_update(const AdamScalars &s, float *params, uint8_t *mc,
+                                            uint8_t *vc, int64_t e, const float (&m)[W],
+                                            const float (&v)[W], const Divisor &dm,
+                                            const Divisor &dv, bool vzero) {
+    float p[W];
+    load_f<W, true>(params, e, p);
+    uint32_t cm = 0, cv = 0;
+#pragma unroll
+    for (int w = 0; w < W; ++w) {
+        p[w] = adam_param(s, p[w], m[w], v[w]);
+        cm |= encode1<DBUF_QUANT_INT8>(quot<EXACT>(m[w], dm)) << (8 * w);
+        cv |= (vzero ? 0u : v_code<EXACT>(v[w], dv)) << (8 * w);
+    }
+    store_f<W>(params, e, p);
+    store_c<W>(mc, e, cm);
+    store_c<W>(vc, e, cv);
+}
+
+// Walk of one lane over its units u = j, j + lanes, ... of a block with `upr`
+// units per row: (row, cu) advances by (dr, dc) with one carry.
+struct UnitWalk {
+    int row, cu, dr, dc, upr;
+    __device__ __forceinline__ UnitWalk(int j, int lanes, int upr_) : upr(upr_) {
+        row = j / upr;
+        cu = j - row * upr;
+        dr = lanes / upr;
+        dc = lanes - dr * upr;
+    }
+    __device__ __forceinline__ void next() {
+        cu += dc;
+        row += dr;
+        if (cu >= upr) {
+            cu -= upr;
+            ++row;
+        }
+    }
+};
+
+template <int W, bool EXACT>
+__device__ __forceinline__ void pass2(const AdamScalars &s, float *params, const float *grads,
+                                      uint8_t *mc, uint8_t *vc, int64_t base, int64_t cols,
+                                      int j, int lanes, int upr, int nu, bool inreg,
+                                      float ms_old, float vs_old, const float (&mr)[kOptUnitsPerLane][W],
+                                      const float (&vr)[kOptUnitsPerLane][W], const Divisor &dm,
+                                      const Divisor &dv, bool vzero) {
+    UnitWalk wk(j, lanes, upr);
+    if (inreg) {
+#pragma unroll
+        for (int i = 0; i < kOptUnitsPerLane; ++i) {
+            if (j + i * lanes < nu)
+                unit_update<W, EXACT>(s, params, mc, vc, base + int64_t(wk.row) * cols + wk.cu * W,
+                                      mr[i], vr[i], dm, dv, vzero);
+            wk.next();
+        }
+    } else {
+        for (int u = j; u < nu; u += lanes) {
+            const int64_t e = base + int64_t(wk.row) * cols + wk.cu * W;
+            float m[W], v[W], ma = 0.0f, va = 0.0f;
+            unit_moments<W, false>(s, grads, mc, vc, e, ms_old, vs_old, m, v, ma, va);
+            unit_update<W, EXACT>(s, params, mc, vc, e, m, v, dm, dv, vzero);
+            wk.next();
+        }
+    }
+}
+
+template <int W>
+__device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it,
+                                         const TensorDesc &d, float *params, const float *grads,
+                                         uint8_t *mc, uint8_t *vc, float *ms, float *vs) {
+    const int lanes = it.lanes;
+    const int sh = __ffs(lanes) - 1;
+    const int groups = kThreads >> sh;
+    const int grp = int(threadIdx.x) >> sh, j = int(threadIdx.x) & (lanes - 1);
+    for (int k0 = 0; k0 < it.count; k0 += groups) {
+        const int k = k0 + grp;
+        const bool active = k < it.count;
+        int64_t base = 0, si = 0;
+        int upr = 1, nu = 0;
+        float ms_old = 0.0f, vs_old = 0.0f;
+        if (active) {
+            const int64_t b = it.first + k;
+            const int64_t bi = b / d.nbc, bj = b - bi * d.nbc;
+            const int64_t r0 = bi * d.qrows, c0 = bj * d.qcols;
+            const int br = int(min(int64_t(d.qrows), d.rows - r0));
+            const int bc = int(min(int64_t(d.qcols), d.cols - c0));
+            base = d.buf_off + r0 * d.cols + c0;
+            upr = bc / W;
+            nu = br * upr;
+            si = d.scale_off + b;
+            ms_old = ms[si];
+            vs_old = vs[si];
+        }
+        const bool inreg = nu <= lanes * kOptUnitsPerLane;
+        float mr[kOptUnitsPerLane][W], vr[kOptUnitsPerLane][W];
+        float mamax = 0.0f, vamax = 0.0f;
+        {
+            UnitWalk wk(j, lanes, upr);
+            if (inreg) {
+#pragma unroll
+                for (int i = 0; i < kOptUnitsPerLane; ++i) {
+                    if (j + i * lanes < nu)
+                        unit_moments<W, true>(s, grads, mc, vc,
+                                              base + int64_t(wk.row) * d.cols + wk.cu * W, ms_old,
+                                              vs_old, mr[i], vr[i], mamax, vamax);
+                    wk.next();
+                }
+            } else {
+                for (int u = j; u < nu; u += lanes) {
+                    float m[W], v[W];
+                    unit_moments<W, false>(s, grads, mc, vc,
+                                           base + int64_t(wk.row) * d.cols + wk.cu * W, ms_old,
+                                           vs_old, m, v, mamax, vamax);
+                    wk.next();
+                }
+            }
+        }
+        for (int o = lanes >> 1; o > 0; o >>= 1) {
+            mamax = fmaxf(mamax, __shfl_xor_sync(0xFFFFFFFFu, mamax, o));
+            vamax = fmaxf(vamax, __shfl_xor_sync(0xFFFFFFFFu, vamax, o));
+        }
+        if (!active) continue;
+        const float ms_new = block_scale(mamax, 127.0f);
+        const float vs_new = __fdiv_rn(vamax, 256.0f);
+        const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
+        const bool vzero = !(vs_new > 0.0f);
+        if (dm.exact || dv.exact)
+            pass2<W, true>(s, params, grads, mc, vc, base, d.cols, j, lanes, upr, nu, inreg, ms_old,
+                           vs_old, mr, vr, dm, dv, vzero);
+        else
+            pass2<W, false>(s, params, grads, mc, vc, base, d.cols, j, lanes, upr, nu, inreg,
+                            ms_old, vs_old, mr, vr, dm, dv, vzero);
+        if (j == 0) {
+            ms[si] = ms_new;
+            vs[si] = vs_new;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kThreads)
+    adamw8_kernel(const Chunk *__restrict__ chunks, const int32_t *__restrict__ plain,
+                  int32_t n_plain, const OptItem *__restrict__ items,
+                  const TensorDesc *__restrict__ td, float *__restrict__ params,
+                  const float *__restrict__ grads, uint8_t *__restrict__ mc,
+                  uint8_t *__restrict__ vc, float *__restrict__ ms, float *__restrict__ vs,
+                  float *__restrict__ m32, float *__restrict__ v32, const dbuf_adamw_hparams hp,
+                  const float *__restrict__ total_norm, const int32_t *__restrict__ nonfinite) {
+    if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
+    const AdamScalars s = adam_scalars(hp, total_norm);
+    if (int(blockIdx.x) < n_plain) {
+        const Chunk c = chunks[plain[blockIdx.x]];
+        const int64_t base = td[c.tensor].buf_off + c.off;
+        const int64_t sb = td[c.tensor].state_off + c.off;
+        adamw_range(s, params + base, grads + base, m32 + sb, v32 + sb, c.len);
+        return;
+    }
+    const OptItem it = items[blockIdx.x - n_plain];
+    const TensorDesc &d = td[it.tensor];
+    const bool vec = d.qcols % 4 == 0 && d.cols % 4 == 0 && d.buf_off % 4 == 0 &&
+                     aligned16(params, grads) &&
+                     ((reinterpret_cast<uintptr_t>(mc) | reinterpret_cast<uintptr_t>(vc)) & 3) == 0;
+    if (vec)
+        opt_item<4>(s, it, d, params, grads, mc, vc, ms, vs);
+    else
+        opt_item<1>(s, it, d, params, grads, mc, vc, ms, vs);
+}
+
 }  // namespace
 
 int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
@@ -122,6 +389,20 @@ int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float 
     adamw_kernel<<<unsigned(p->chunks.size()), kThreads, 0, st>>>(
         p->dev.chunks, p->dev.tensors, params, grads, exp_avg, exp_avg_sq, hp, total_norm,
         nonfinite);
+    return cudaGetLastError();
+}
+
+int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8_t *m_codes,
+                  uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
+                  const dbuf_adamw_hparams &hp, const float *total_norm, const int32_t *nonfinite,
+                  void *stream) {
+    const size_t grid = p->opt_plain.size() + p->opt_items.size();
+    if (grid == 0) return cudaSuccess;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    adamw8_kernel<<<unsigned(grid), kThreads, 0, st>>>(
+        p->dev.chunks, p->dev.opt_plain, int32_t(p->opt_plain.size()), p->dev.opt_items,
+        p->dev.tensors, params, grads, m_codes, v_codes, m_scales, v_scales, m32, v32, hp,
+        total_norm, nonfinite);
     return cudaGetLastError();
 }
 

@@ -209,6 +209,11 @@ int validate(const dbuf_tensor_spec *specs, int32_t n, int32_t m, const int32_t 
             const int64_t qr = s.qblock_rows > 0 ? s.qblock_rows : std::max<int64_t>(s.rows, 1);
             const bool cuttable = s.gran_rows > 0 && s.gran_rows < s.rows;
             if (cuttable && s.gran_rows % qr != 0) return DBUF_EINVAL;
+            // elements of one block are counted with 32-bit integers
+            const int64_t qc = s.qblock_cols > 0 ? s.qblock_cols : std::max<int64_t>(s.cols, 1);
+            if (std::min(qr, std::max<int64_t>(s.rows, 1)) * std::min(qc, std::max<int64_t>(s.cols, 1)) >=
+                (int64_t(1) << 31))
+                return DBUF_ERANGE;
         }
     }
     return DBUF_OK;
@@ -223,7 +228,10 @@ void build_tables(dbuf_plan_t *p) {
     p->tile_items.clear();
     p->pipe_items.clear();
     p->pipe_tensors.clear();
-    int64_t s_off = 0;
+    p->opt_items.clear();
+    p->opt_plain.clear();
+    p->state_offsets.assign(n, -1);
+    int64_t s_off = 0, st_off = 0;
     for (int32_t t = 0; t < n; ++t) {
         const dbuf_tensor_spec &s = p->specs[t];
         TensorDesc &d = p->tdesc[t];
@@ -241,9 +249,35 @@ void build_tables(dbuf_plan_t *p) {
         for (int64_t o = 0; o < d.numel; o += dbuf::kChunkElems)
             p->chunks.push_back(Chunk{o, t, int32_t(std::min(dbuf::kChunkElems, d.numel - o))});
         d.chunk_end = int32_t(p->chunks.size());
+        d.state_off = -1;
+        if (s.quant == DBUF_QUANT_NONE) {
+            // compact fp32 moments of the 8-bit optimizer, 16-byte aligned starts
+            d.state_off = st_off;
+            p->state_offsets[t] = st_off;
+            st_off += (d.numel + 3) / 4 * 4;
+            for (int32_t c = d.chunk_begin; c < d.chunk_end; ++c) p->opt_plain.push_back(c);
+        }
         if (s.quant != DBUF_QUANT_NONE && d.numel > 0) {
             const int64_t nbr = (s.rows + d.qrows - 1) / d.qrows;
             const int64_t nb = nbr * d.nbc;
+            {
+                // 8-bit optimizer items: the fewest lanes per block that keep the
+                // block's moments in registers (units of 4 elements when rows and
+                // block widths allow vector access), 32 lanes and a recompute pass
+                // for larger blocks; about kOptItemElems elements per item.
+                const int64_t be = int64_t(d.qrows) * d.qcols;
+                const bool vec = d.qcols % 4 == 0 && s.cols % 4 == 0 && d.buf_off % 4 == 0;
+                const int64_t units = vec ? be / 4 : be;
+                int lanes = 4;
+                while (lanes < 32 && units > int64_t(lanes) * dbuf::kOptUnitsPerLane) lanes *= 2;
+                const int64_t groups = 256 / lanes;
+                int64_t per = std::max<int64_t>(1, dbuf::kOptItemElems / std::max<int64_t>(1, be));
+                per = std::max<int64_t>(groups, (per + groups - 1) / groups * groups);
+                per = std::min<int64_t>(per, 16384);
+                for (int64_t b = 0; b < nb; b += per)
+                    p->opt_items.push_back(dbuf::OptItem{b, t, int16_t(std::min(per, nb - b)),
+                                                         int16_t(lanes)});
+            }
             if (d.qrows == 1) {
                 for (int64_t b = 0; b < nb; b += dbuf::kRowItemBlocks)
                     p->row_items.push_back(dbuf::RowItem{
@@ -272,6 +306,7 @@ void build_tables(dbuf_plan_t *p) {
         }
     }
     p->n_scales = s_off;
+    p->n_state = st_off;
 }
 
 }  // namespace
@@ -349,7 +384,8 @@ extern "C" int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
         for (int k = 0; k <= m; ++k) p->bounds[k] = S * c[k];
         build_tables(p);
         if (p->chunks.size() > size_t(INT32_MAX) || p->tile_items.size() > size_t(INT32_MAX) ||
-            p->row_items.size() > size_t(INT32_MAX) || p->pipe_items.size() > size_t(INT32_MAX)) {
+            p->row_items.size() > size_t(INT32_MAX) || p->pipe_items.size() > size_t(INT32_MAX) ||
+            p->opt_items.size() + p->opt_plain.size() > size_t(INT32_MAX)) {
             delete p;
             return DBUF_ERANGE;
         }
@@ -372,6 +408,15 @@ extern "C" int dbuf_plan_query(const dbuf_plan_t *p, int64_t *S, int64_t *total,
     if (scale_offsets && p->n)
         std::memcpy(scale_offsets, p->scale_offsets.data(), sizeof(int64_t) * p->n);
     if (n_scales) *n_scales = p->n_scales;
+    return DBUF_OK;
+}
+
+extern "C" int dbuf_plan_state_offsets(const dbuf_plan_t *p, int64_t *state_offsets,
+                                       int64_t *n_state) {
+    if (!p) return DBUF_EINVAL;
+    if (state_offsets && p->n)
+        std::memcpy(state_offsets, p->state_offsets.data(), sizeof(int64_t) * p->n);
+    if (n_state) *n_state = p->n_state;
     return DBUF_OK;
 }
 

@@ -44,7 +44,8 @@ _QUANT = {None: DBUF_QUANT_NONE, "none": DBUF_QUANT_NONE, "e4m3": DBUF_QUANT_E4M
 EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
-           "dbuf_device_status", "dbuf_adamw_step", "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_device_status", "dbuf_adamw_step", "dbuf_plan_state_offsets",
+           "dbuf_adamw8_step", "dbuf_strerror", "dbuf_last_cuda_error")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -112,6 +113,10 @@ def _lib_handle():
         L.dbuf_block_quant.restype = ctypes.c_int
         L.dbuf_adamw_step.argtypes = [P, P, P, P, P, P, P, P, P]
         L.dbuf_adamw_step.restype = ctypes.c_int
+        L.dbuf_plan_state_offsets.argtypes = [P, P, P]
+        L.dbuf_plan_state_offsets.restype = ctypes.c_int
+        L.dbuf_adamw8_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
+        L.dbuf_adamw8_step.restype = ctypes.c_int
         L.dbuf_device_status.argtypes = [P, P, P]
         L.dbuf_device_status.restype = ctypes.c_int
         L.dbuf_strerror.argtypes = [ctypes.c_int]
@@ -230,6 +235,33 @@ def dbuf_adamw_step(plan: int, params: int, grads: int, exp_avg: int, exp_avg_sq
     _check(_lib_handle().dbuf_adamw_step(plan, params, grads, exp_avg, exp_avg_sq,
                                          ctypes.byref(hp), total_norm or None, nonfinite or None,
                                          stream), "dbuf_adamw_step")
+
+
+def dbuf_plan_state_offsets(plan: int, n: int):
+    """(state_offsets[n], n_state) of the compact fp32 moments of the 8-bit step."""
+    off = (ctypes.c_int64 * max(n, 1))()
+    ns = ctypes.c_int64()
+    _check(_lib_handle().dbuf_plan_state_offsets(plan, off, ctypes.byref(ns)),
+           "dbuf_plan_state_offsets")
+    return list(off)[:n], ns.value
+
+
+def dbuf_adamw8_step(plan: int, params: int, grads: int, exp_avg_codes: int,
+                     exp_avg_sq_codes: int, exp_avg_scales: int, exp_avg_sq_scales: int,
+                     exp_avg_fp32: int, exp_avg_sq_fp32: int, *, lr: float, beta1: float,
+                     beta2: float, eps: float, weight_decay: float, bias_correction1: float,
+                     bias_correction2: float, max_norm: float = 0.0, total_norm: int = 0,
+                     nonfinite: int = 0, stream: int = 0) -> None:
+    """One 8-bit AdamW step (block-quantised moments); pointers as in dbuf.h,
+    0 for the optional ones."""
+    hp = dbuf_adamw_hparams(lr, beta1, beta2, eps, weight_decay, bias_correction1,
+                            bias_correction2, max_norm)
+    _check(_lib_handle().dbuf_adamw8_step(plan, params, grads, exp_avg_codes or None,
+                                          exp_avg_sq_codes or None, exp_avg_scales or None,
+                                          exp_avg_sq_scales or None, exp_avg_fp32 or None,
+                                          exp_avg_sq_fp32 or None, ctypes.byref(hp),
+                                          total_norm or None, nonfinite or None, stream),
+           "dbuf_adamw8_step")
 
 
 def dbuf_device_status(plan: int, stream: int = 0) -> int:

@@ -43,6 +43,7 @@ class DBuffer:
         self.shard_bounds: List[int] = q["shard_bounds"]
         self.scale_offsets: List[int] = q["scale_offsets"]
         self.n_scales: int = q["n_scales"]
+        self.state_offsets, self.n_state = _c.dbuf_plan_state_offsets(self.handle, self.n)
         self.numel = [int(s.rows) * int(s.cols) if not isinstance(s, (tuple, list))
                       else int(s[0]) * int(s[1]) for s in self.specs]
         dev = torch.device(device if device is not None else "cuda")
@@ -192,3 +193,45 @@ class DBuffer:
                            total_norm=total_norm.data_ptr() if total_norm is not None else 0,
                            nonfinite=nonfinite.data_ptr() if nonfinite is not None else 0,
                            stream=self._stream(stream))
+
+    # -- 8-bit AdamW -----------------------------------------------------------
+    def new_adamw8_state(self) -> Dict[str, torch.Tensor]:
+        """Zero 8-bit AdamW state: uint8 codes of m and v in the flat buffer's
+        layout, fp32 block scales, compact fp32 moments of unquantised tensors."""
+        def z(n, dt):
+            return torch.zeros(max(n, 1), dtype=dt, device=self.device)
+        return {"m_codes": z(self.total, torch.uint8), "v_codes": z(self.total, torch.uint8),
+                "m_scales": z(self.n_scales, torch.float32),
+                "v_scales": z(self.n_scales, torch.float32),
+                "m32": z(self.n_state, torch.float32), "v32": z(self.n_state, torch.float32)}
+
+    def adamw8_step(self, params: torch.Tensor, grads: torch.Tensor, state: Dict[str, torch.Tensor],
+                    *, step: int, lr: float, betas=(0.9, 0.999), eps: float = 1e-8,
+                    weight_decay: float = 0.0, max_norm: float = 0.0,
+                    total_norm: Optional[torch.Tensor] = None,
+                    nonfinite: Optional[torch.Tensor] = None, stream=None) -> None:
+        """One fused 8-bit AdamW step (step >= 1) on the state of new_adamw8_state."""
+        for b in (params, grads):
+            self._check_buf(b)
+            if b.dtype != torch.float32:
+                raise TypeError("AdamW parameters and gradients are float32")
+        need = {"m_codes": (self.total, torch.uint8), "v_codes": (self.total, torch.uint8),
+                "m_scales": (self.n_scales, torch.float32),
+                "v_scales": (self.n_scales, torch.float32),
+                "m32": (self.n_state, torch.float32), "v32": (self.n_state, torch.float32)}
+        for k, (n, dt) in need.items():
+            t = state[k]
+            if t.dtype != dt or t.numel() < n or not t.is_contiguous() or t.device != self.device:
+                raise ValueError(f"8-bit AdamW state {k}: want {n} {dt} on {self.device}")
+        b1, b2 = betas
+        _c.dbuf_adamw8_step(self.handle, params.data_ptr(), grads.data_ptr(),
+                            state["m_codes"].data_ptr(), state["v_codes"].data_ptr(),
+                            state["m_scales"].data_ptr(), state["v_scales"].data_ptr(),
+                            state["m32"].data_ptr(), state["v32"].data_ptr(), lr=lr, beta1=b1,
+                            beta2=b2, eps=eps, weight_decay=weight_decay,
+                            bias_correction1=1.0 - b1 ** step, bias_correction2=1.0 - b2 ** step,
+                            max_norm=max_norm,
+                            total_norm=total_norm.data_ptr() if total_norm is not None else 0,
+                            nonfinite=nonfinite.data_ptr() if nonfinite is not None else 0,
+                            stream=self._stream(stream))
+

@@ -327,6 +327,55 @@ int dbuf_adamw_step(const dbuf_plan_t *plan, float *params, const float *grads, 
                     float *exp_avg_sq, const dbuf_adamw_hparams *hp, const float *total_norm,
                     const int32_t *nonfinite, void *stream);
 
+/*
+ * dbuf_plan_state_offsets -- layout of the compact fp32 moments that
+ * dbuf_adamw8_step keeps for tensors without a quantisation block (vectors,
+ * norm weights): those tensors in group order, each starting at a multiple of
+ * 4 elements.  state_offsets[n] receives each tensor's first element (-1 for
+ * quantised tensors), *n_state the elements per moment buffer.  Either pointer
+ * may be NULL.  Errors: DBUF_EINVAL (plan NULL).
+ */
+int dbuf_plan_state_offsets(const dbuf_plan_t *plan, int64_t *state_offsets, int64_t *n_state);
+
+/*
+ * dbuf_adamw8_step -- 8-bit AdamW over the group, one launch.
+ * [veScale-FSDP §6.3 8-bit Adam: block-wise INT8 quantisation of the
+ * optimizer's gradient statistics; the per-parameter block shape set through
+ * orig_param_policy; blocks never cross a shard, so each shard quantises its
+ * own moments without communication.]  The section does not give the code
+ * maps; this library reads them as:
+ *   m = code_m * scale_m, code_m int8 in [-127, 127], scale_m = amax|m| / 127
+ *       (1 when not positive) -- the INT8 map of dbuf_block_quant;
+ *   v = (code_v + 1) * scale_v, code_v uint8 in [0, 255], scale_v = amax(v) / 256
+ *       -- no zero level, so a positive v never dequantises to 0 (the update
+ *       would otherwise become m / eps); an all-zero block has scale 0, codes 0.
+ * For every tensor with a quantisation block (spec quant != NONE; its block
+ * shape, whatever the spec's own code type), per block: dequantise (one fp32
+ * multiply each), the AdamW step of dbuf_adamw_step in the same fp32 operation
+ * order, new scales from the new moments' block maxima, codes =
+ * clamp(rint(m / scale_m), -127, 127) and clamp(rint(v / scale_v), 1, 256) - 1
+ * with the quotients correctly rounded.  Tensors without a quantisation block
+ * take the fp32 step on compact fp32 moments (dbuf_plan_state_offsets).
+ *   params, grads: device fp32 buffers with the plan's layout (params updated
+ *     in place; grads e.g. the accumulator).
+ *   exp_avg_codes, exp_avg_sq_codes: device uint8 buffers of the plan's total
+ *     size, the flat buffer's layout; only quantised tensors' ranges are read
+ *     and written.  Zero codes with zero scales are the zero state.
+ *   exp_avg_scales, exp_avg_sq_scales: device fp32, n_scales each, indexed like
+ *     dbuf_block_quant's scales.
+ *   exp_avg_fp32, exp_avg_sq_fp32: device fp32, n_state each (may be NULL when
+ *     n_state is 0).
+ * hp, total_norm and nonfinite as for dbuf_adamw_step (clipping from a device
+ * norm; a set non-finite flag skips the step and nothing is written).
+ * Errors: DBUF_EINVAL (null pointers, non-positive bias corrections),
+ * DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_adamw8_step(const dbuf_plan_t *plan, float *params, const float *grads,
+                     uint8_t *exp_avg_codes, uint8_t *exp_avg_sq_codes, float *exp_avg_scales,
+                     float *exp_avg_sq_scales, float *exp_avg_fp32, float *exp_avg_sq_fp32,
+                     const dbuf_adamw_hparams *hp, const float *total_norm,
+                     const int32_t *nonfinite, void *stream);
+
 /* dbuf_strerror -- static description of a return code. */
 const char *dbuf_strerror(int code);
 

@@ -50,6 +50,12 @@ def test_plan_rejects_bad_arguments(dbuf_lib):
     with pytest.raises(d.DbufError) as e:
         d.dbuf_plan([(1 << 40, 1 << 20, 1)], 2)
     assert e.value.code == d.DBUF_ERANGE
+    # one quantisation block of 2^31 elements or more
+    with pytest.raises(d.DbufError) as e:
+        d.dbuf_plan([(1 << 16, 1 << 15, 0, (0, 0), "int8")], 2)
+    assert e.value.code == d.DBUF_ERANGE
+    p = d.dbuf_plan([(1 << 16, (1 << 15) - 1, 0, (0, 0), "int8")], 2)
+    d.dbuf_plan_free(p)
 
 
 def test_operators_refuse_unuploaded_plan_without_gpu(dbuf_lib):
@@ -60,7 +66,10 @@ def test_operators_refuse_unuploaded_plan_without_gpu(dbuf_lib):
                      lambda: d.dbuf_unpack(p, 0, d.DBUF_F32, 0, d.DBUF_F32),
                      lambda: d.dbuf_scale_accum_zero(p, 0, d.DBUF_F32, 0, 0.5),
                      lambda: d.dbuf_norm_nonfinite(p, 0, d.DBUF_F32, 0, 0, 0, 0, 0),
-                     lambda: d.dbuf_block_quant(p, 0, 0, 0)]:
+                     lambda: d.dbuf_block_quant(p, 0, 0, 0),
+                     lambda: d.dbuf_adamw8_step(p, 0, 0, 0, 0, 0, 0, 0, 0, lr=1e-3, beta1=0.9,
+                                                beta2=0.95, eps=1e-8, weight_decay=0.0,
+                                                bias_correction1=0.1, bias_correction2=0.05)]:
             with pytest.raises(d.DbufError) as e:
                 call()
             assert e.value.code == d.DBUF_ENOTUPLOADED

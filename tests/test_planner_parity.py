@@ -1,5 +1,5 @@
 """The C++ planner in libdbuf equals the oracle byte for byte (S, offsets, shard
-bounds, scale offsets) on the five workloads and on random groups, and plans
+bounds, scale offsets, 8-bit optimizer state offsets) on the five workloads and on random groups, and plans
 within the pages' runtime figure (under 0.3 s) -- host only, no GPU."""
 import random
 import time
@@ -13,7 +13,9 @@ from workloads.configs import TensorSpec, random_tiny_group
 def _cplan(d, specs, m, units=None, align=16):
     p = d.dbuf_plan(specs, m, units, align)
     try:
-        return d.dbuf_plan_query(p, len(specs), m)
+        q = d.dbuf_plan_query(p, len(specs), m)
+        q["state_offsets"], q["n_state"] = d.dbuf_plan_state_offsets(p, len(specs))
+        return q
     finally:
         d.dbuf_plan_free(p)
 
@@ -25,6 +27,8 @@ def _same(q, o, specs, oracle_lib):
     assert q["shard_bounds"] == [int(x) for x in o.bounds]
     soff, ns = oracle_lib.scale_offsets(specs)
     assert q["scale_offsets"] == [int(x) for x in soff] and q["n_scales"] == ns
+    st, nst = oracle_lib.state_offsets(specs)
+    assert q["state_offsets"] == [int(x) for x in st] and q["n_state"] == nst
 
 
 @pytest.mark.parametrize("key", list(WORKLOADS))

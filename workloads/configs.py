@@ -188,6 +188,15 @@ def _mixed_group(seed: int = 0, count: int = 2000) -> Workload:
         grad_dtype=torch.float32, seed=seed)
 
 
+def adam8_group(group: GroupSpec, block=(32, 32)) -> GroupSpec:
+    """The group as the 8-bit Adam experiment shards it: every matrix with
+    block x block INT8 quantisation blocks and block[0]-row sharding
+    granularity; other tensors unchanged."""
+    ts = tuple(TensorSpec(t.name, t.rows, t.cols, block[0], tuple(block), "int8", t.kind)
+               if t.kind == "matrix" else t for t in group.tensors)
+    return GroupSpec(group.name + "_adam8", ts, group.repeat)
+
+
 WORKLOADS = {
     "tiny": _tiny_transformer,
     "llama_layer": _llama_layer,
