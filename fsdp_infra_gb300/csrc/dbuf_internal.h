@@ -75,19 +75,20 @@ struct TileItem {
 static_assert(sizeof(TileItem) == 16, "TileItem layout");
 
 // A run of `count` consecutive quantisation blocks (row-major block order) of
-// one tensor for the 8-bit optimizer step, starting at block `first`; `lanes`
-// threads (4, 8, 16 or 32) work on one block.
+// one tensor for the 8-bit optimizer step, starting at block (bi0, bj0);
+// `lanes` threads (a power of two from 4 to 256) work on one block.
 struct OptItem {
-    int64_t first;
     int32_t tensor;
+    int32_t bi0;
+    int32_t bj0;
     int16_t count;
     int16_t lanes;
 };
 static_assert(sizeof(OptItem) == 16, "OptItem layout");
 
-// Moment units (4 elements on the vector path) that one lane of the 8-bit
+// Moment units (4 elements on the vector path) that one thread of the 8-bit
 // optimizer keeps in registers; larger blocks are recomputed in a second pass.
-constexpr int kOptUnitsPerLane = 8;
+constexpr int kOptUnitsPerLane = 2;
 // Target elements per 8-bit optimizer work item.
 constexpr int64_t kOptItemElems = 16384;
 

@@ -146,6 +146,63 @@ __global__ void __launch_bounds__(kThreads)
 // 8-bit AdamW
 // ---------------------------------------------------------------------------
 
+// AdamW over `len` fp32 elements, one float4 per thread per iteration: the
+// unquantised tensors of the 8-bit step (norm weights, biases) are small, and
+// this body keeps the launch's register count at the block path's.
+__device__ __forceinline__ void adamw_range_lean(const AdamScalars &s, float *p, const float *g,
+                                                 float *m, float *v, int len) {
+    const bool vec = aligned16(p, g) && aligned16(m, v);
+    const int nv = vec ? len / 4 : 0;
+    for (int i = int(threadIdx.x); i < nv; i += kThreads) {
+        float4 pp = __ldcs(reinterpret_cast<const float4 *>(p) + i);
+        const float4 gg = __ldcs(reinterpret_cast<const float4 *>(g) + i);
+        float4 mm = __ldcs(reinterpret_cast<const float4 *>(m) + i);
+        float4 vv = __ldcs(reinterpret_cast<const float4 *>(v) + i);
+        adam_elem(s, pp.x, gg.x, mm.x, vv.x);
+        adam_elem(s, pp.y, gg.y, mm.y, vv.y);
+        adam_elem(s, pp.z, gg.z, mm.z, vv.z);
+        adam_elem(s, pp.w, gg.w, mm.w, vv.w);
+        __stcs(reinterpret_cast<float4 *>(p) + i, pp);
+        __stcs(reinterpret_cast<float4 *>(m) + i, mm);
+        __stcs(reinterpret_cast<float4 *>(v) + i, vv);
+    }
+    for (int i = nv * 4 + int(threadIdx.x); i < len; i += kThreads) {
+        float pe = p[i], me = m[i], ve = v[i];
+        adam_elem(s, pe, g[i], me, ve);
+        p[i] = pe;
+        m[i] = me;
+        v[i] = ve;
+    }
+}
+
+// Exact conversions through the fp32 significand.  A byte u placed under the
+// exponent of 2^23 (bits 0x4B0000uu) is the float 2^23 + u.  For |q| < 2^22,
+// RN(q + 1.5*2^23) is 1.5*2^23 + rint(q) with ties to even (fp32 spacing is 1
+// in [2^23, 2^24)), and its bits are 0x4B400000 + rint(q), so the low byte is
+// rint(q) mod 256.
+constexpr float kMagicRound = 12582912.0f;     // 1.5 * 2^23
+constexpr uint32_t kMagicByte = 0x4B000000u;   // 2^23
+
+__device__ __forceinline__ float2 splat(float a) { return make_float2(a, a); }
+
+// Packed fp32x2 operations are used only where no packed multiply feeds a
+// packed add: the compiler fuses such a pair into one fp32x2 multiply-add (a
+// single rounding) even when both carry an explicit round-to-nearest modifier,
+// which the scalar __fmul_rn / __fadd_rn never are.  Dequantisation (add, then
+// multiply) and encoding (multiply-add, then add) are safe; the moment and
+// parameter updates use the scalar forms.
+
+__device__ __forceinline__ float byte_float(uint32_t w, int k) {
+    return __uint_as_float(__byte_perm(w, kMagicByte, 0x7650u | unsigned(k)));
+}
+
+// The low bytes of four floats' bits, packed into one word.
+__device__ __forceinline__ uint32_t low_bytes(float a, float b, float c, float d) {
+    const uint32_t ab = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x0040u);
+    const uint32_t cd = __byte_perm(__float_as_uint(c), __float_as_uint(d), 0x0040u);
+    return __byte_perm(ab, cd, 0x5410u);
+}
+
 // A lane's unit is W consecutive elements of one block row (W = 4 on the
 // vector path).  STREAM marks loads of data read once (evict-first).
 template <int W, bool STREAM>
@@ -185,7 +242,8 @@ __device__ __forceinline__ void store_c(uint8_t *c, int64_t e, uint32_t x) {
         c[e] = uint8_t(x);
 }
 
-// Dequantise a unit's codes and step its moments; updates the block maxima.
+// Dequantise a unit's codes (m = code * scale, v = (code + 1) * scale) and
+// step its moments; updates the block maxima.
 template <int W, bool STREAM>
 __device__ __forceinline__ void unit_moments(const AdamScalars &s, const float *grads,
                                              const uint8_t *mc, const uint8_t *vc, int64_t e,
@@ -194,13 +252,29 @@ __device__ __forceinline__ void unit_moments(const AdamScalars &s, const float *
     float g[W];
     load_f<W, STREAM>(grads, e, g);
     const uint32_t cm = load_c<W, STREAM>(mc, e), cv = load_c<W, STREAM>(vc, e);
+    if constexpr (W == 4) {
+        // int8 c: the byte c ^ 0x80 = c + 128, so c = (2^23 + c + 128) - (2^23 + 128)
+        const uint32_t xm = cm ^ 0x80808080u;
+        const float2 om = splat(-8388736.0f), ov = splat(-8388607.0f);
+        const float2 sm = splat(ms_old), sv = splat(vs_old);
+        float2 m01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 0), byte_float(xm, 1)), om), sm);
+        float2 m23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 2), byte_float(xm, 3)), om), sm);
+        float2 v01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cv, 0), byte_float(cv, 1)), ov), sv);
+        float2 v23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cv, 2), byte_float(cv, 3)), ov), sv);
+        m[0] = m01.x; m[1] = m01.y; m[2] = m23.x; m[3] = m23.y;
+        v[0] = v01.x; v[1] = v01.y; v[2] = v23.x; v[3] = v23.y;
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-        m[w] = __fmul_rn(__int2float_rn(int(int8_t(uint8_t(cm >> (8 * w))))), ms_old);
-        v[w] = __fmul_rn(__int2float_rn(int((cv >> (8 * w)) & 0xFFu) + 1), vs_old);
-        adam_moments(s, g[w], m[w], v[w]);
-        mamax = fmaxf(mamax, fabsf(m[w]));
-        vamax = fmaxf(vamax, v[w]);
+        for (int w = 0; w < 4; ++w) adam_moments(s, g[w], m[w], v[w]);
+        mamax = fmaxf(fmaxf(mamax, fabsf(m[0])), fmaxf(fabsf(m[1]), fabsf(m[2])));
+        mamax = fmaxf(mamax, fabsf(m[3]));
+        vamax = fmaxf(fmaxf(vamax, v[0]), fmaxf(v[1], v[2]));
+        vamax = fmaxf(vamax, v[3]);
+    } else {
+        m[0] = __fmul_rn(__int2float_rn(int(int8_t(uint8_t(cm)))), ms_old);
+        v[0] = __fmul_rn(__int2float_rn(int(cv & 0xFFu) + 1), vs_old);
+        adam_moments(s, g[0], m[0], v[0]);
+        mamax = fmaxf(mamax, fabsf(m[0]));
+        vamax = fmaxf(vamax, v[0]);
     }
 }
 
@@ -211,20 +285,43 @@ __device__ __forceinline__ uint32_t v_code(float v, const Divisor &d) {
     return uint32_t(min(256, max(1, c)) - 1);
 }
 
-// Pass 2 of one unit: parameters, then both codes.
+// Pass 2 of one unit: parameters from the new moments, then both codes.  The
+// reciprocal-step path (!EXACT: both scales in [2^-80, 2^100]) rounds through
+// the magic constant: |m / scale_m| <= 127 (1 + 2^-24) and 0 <= v / scale_v <=
+// 256 there, so no clamp can bind beyond max(q, 1) for v.
 template <int W, bool EXACT>
 __device__ __forceinline__ void unit_update(const AdamScalars &s, float *params, uint8_t *mc,
-                                            uint8_t *vc, int64_t e, const float (&m)[W],
-                                            const float (&v)[W], const Divisor &dm,
-                                            const Divisor &dv, bool vzero) {
+                                            uint8_t *vc, int64_t e, const float (&pin)[W],
+                                            const float (&m)[W], const float (&v)[W],
+                                            const Divisor &dm, const Divisor &dv, bool vzero) {
     float p[W];
-    load_f<W, true>(params, e, p);
     uint32_t cm = 0, cv = 0;
+    if constexpr (W == 4) {
 #pragma unroll
-    for (int w = 0; w < W; ++w) {
-        p[w] = adam_param(s, p[w], m[w], v[w]);
-        cm |= encode1<DBUF_QUANT_INT8>(quot<EXACT>(m[w], dm)) << (8 * w);
-        cv |= (vzero ? 0u : v_code<EXACT>(v[w], dv)) << (8 * w);
+        for (int w = 0; w < 4; ++w) p[w] = adam_param(s, pin[w], m[w], v[w]);
+        if (!EXACT) {
+            const float2 mg = splat(kMagicRound);
+            const float2 qm01 = __fadd2_rn(quot2(make_float2(m[0], m[1]), dm), mg);
+            const float2 qm23 = __fadd2_rn(quot2(make_float2(m[2], m[3]), dm), mg);
+            cm = low_bytes(qm01.x, qm01.y, qm23.x, qm23.y);
+            float2 qv01 = quot2(make_float2(v[0], v[1]), dv);
+            float2 qv23 = quot2(make_float2(v[2], v[3]), dv);
+            qv01 = make_float2(fmaxf(qv01.x, 1.0f), fmaxf(qv01.y, 1.0f));
+            qv23 = make_float2(fmaxf(qv23.x, 1.0f), fmaxf(qv23.y, 1.0f));
+            qv01 = __fadd2_rn(__fadd2_rn(qv01, mg), splat(-1.0f));
+            qv23 = __fadd2_rn(__fadd2_rn(qv23, mg), splat(-1.0f));
+            cv = low_bytes(qv01.x, qv01.y, qv23.x, qv23.y);
+        } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                cm |= encode1<DBUF_QUANT_INT8>(quot<true>(m[w], dm)) << (8 * w);
+                cv |= (vzero ? 0u : v_code<true>(v[w], dv)) << (8 * w);
+            }
+        }
+    } else {
+        p[0] = adam_param(s, pin[0], m[0], v[0]);
+        cm = encode1<DBUF_QUANT_INT8>(quot<EXACT>(m[0], dm));
+        cv = vzero ? 0u : v_code<EXACT>(v[0], dv);
     }
     store_f<W>(params, e, p);
     store_c<W>(mc, e, cm);
@@ -254,96 +351,129 @@ struct UnitWalk {
 template <int W, bool EXACT>
 __device__ __forceinline__ void pass2(const AdamScalars &s, float *params, const float *grads,
                                       uint8_t *mc, uint8_t *vc, int64_t base, int64_t cols,
-                                      int j, int lanes, int upr, int nu, bool inreg,
-                                      float ms_old, float vs_old, const float (&mr)[kOptUnitsPerLane][W],
+                                      int j, int lanes, UnitWalk wk, int nu, bool inreg,
+                                      float ms_old, float vs_old,
+                                      const float (&pr)[kOptUnitsPerLane][W],
+                                      const float (&mr)[kOptUnitsPerLane][W],
                                       const float (&vr)[kOptUnitsPerLane][W], const Divisor &dm,
                                       const Divisor &dv, bool vzero) {
-    UnitWalk wk(j, lanes, upr);
     if (inreg) {
 #pragma unroll
         for (int i = 0; i < kOptUnitsPerLane; ++i) {
             if (j + i * lanes < nu)
                 unit_update<W, EXACT>(s, params, mc, vc, base + int64_t(wk.row) * cols + wk.cu * W,
-                                      mr[i], vr[i], dm, dv, vzero);
+                                      pr[i], mr[i], vr[i], dm, dv, vzero);
             wk.next();
         }
     } else {
         for (int u = j; u < nu; u += lanes) {
             const int64_t e = base + int64_t(wk.row) * cols + wk.cu * W;
-            float m[W], v[W], ma = 0.0f, va = 0.0f;
+            float p[W], m[W], v[W], ma = 0.0f, va = 0.0f;
+            load_f<W, true>(params, e, p);
             unit_moments<W, false>(s, grads, mc, vc, e, ms_old, vs_old, m, v, ma, va);
-            unit_update<W, EXACT>(s, params, mc, vc, e, m, v, dm, dv, vzero);
+            unit_update<W, EXACT>(s, params, mc, vc, e, p, m, v, dm, dv, vzero);
             wk.next();
         }
     }
 }
 
+// One work item: groups of `lanes` threads take its blocks in rounds.  Pass 1
+// loads every unit of the block (parameters too, when the block fits in
+// registers), pass 2 computes and stores; the block maxima meet by shuffles
+// within a warp and through shared memory across warps (lanes > 32), with the
+// slots alternating between rounds so that one barrier per round suffices.
 template <int W>
 __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it,
                                          const TensorDesc &d, float *params, const float *grads,
-                                         uint8_t *mc, uint8_t *vc, float *ms, float *vs) {
+                                         uint8_t *mc, uint8_t *vc, float *ms, float *vs,
+                                         float2 (*red)[kThreads / 32]) {
+    constexpr int U = kOptUnitsPerLane;
     const int lanes = it.lanes;
     const int sh = __ffs(lanes) - 1;
     const int groups = kThreads >> sh;
-    const int grp = int(threadIdx.x) >> sh, j = int(threadIdx.x) & (lanes - 1);
-    for (int k0 = 0; k0 < it.count; k0 += groups) {
+    const int tid = int(threadIdx.x);
+    const int grp = tid >> sh, j = tid & (lanes - 1);
+    const int nbc = d.nbc;
+    // the walk over a full-width block, shared by all but the right-edge blocks
+    const UnitWalk wfull(j, lanes, d.qcols / W);
+    int par = 0;
+    for (int k0 = 0; k0 < it.count; k0 += groups, par ^= 1) {
         const int k = k0 + grp;
         const bool active = k < it.count;
         int64_t base = 0, si = 0;
         int upr = 1, nu = 0;
         float ms_old = 0.0f, vs_old = 0.0f;
+        UnitWalk wk = wfull;
         if (active) {
-            const int64_t b = it.first + k;
-            const int64_t bi = b / d.nbc, bj = b - bi * d.nbc;
-            const int64_t r0 = bi * d.qrows, c0 = bj * d.qcols;
+            int bi = it.bi0, bj = it.bj0 + k;
+            if (bj >= nbc) {
+                const int q = bj / nbc;
+                bi += q;
+                bj -= q * nbc;
+            }
+            const int64_t r0 = int64_t(bi) * d.qrows;
+            const int c0 = bj * d.qcols;
             const int br = int(min(int64_t(d.qrows), d.rows - r0));
             const int bc = int(min(int64_t(d.qcols), d.cols - c0));
             base = d.buf_off + r0 * d.cols + c0;
             upr = bc / W;
             nu = br * upr;
-            si = d.scale_off + b;
+            if (bc != d.qcols) wk = UnitWalk(j, lanes, upr);
+            si = d.scale_off + int64_t(bi) * nbc + bj;
             ms_old = ms[si];
             vs_old = vs[si];
         }
-        const bool inreg = nu <= lanes * kOptUnitsPerLane;
-        float mr[kOptUnitsPerLane][W], vr[kOptUnitsPerLane][W];
+        const bool inreg = nu <= lanes * U;
+        float pr[U][W], mr[U][W], vr[U][W];
         float mamax = 0.0f, vamax = 0.0f;
         {
-            UnitWalk wk(j, lanes, upr);
+            UnitWalk w1 = wk;
             if (inreg) {
 #pragma unroll
-                for (int i = 0; i < kOptUnitsPerLane; ++i) {
-                    if (j + i * lanes < nu)
-                        unit_moments<W, true>(s, grads, mc, vc,
-                                              base + int64_t(wk.row) * d.cols + wk.cu * W, ms_old,
-                                              vs_old, mr[i], vr[i], mamax, vamax);
-                    wk.next();
+                for (int i = 0; i < U; ++i) {
+                    if (j + i * lanes < nu) {
+                        const int64_t e = base + int64_t(w1.row) * d.cols + w1.cu * W;
+                        load_f<W, true>(params, e, pr[i]);
+                        unit_moments<W, true>(s, grads, mc, vc, e, ms_old, vs_old, mr[i], vr[i],
+                                              mamax, vamax);
+                    }
+                    w1.next();
                 }
             } else {
                 for (int u = j; u < nu; u += lanes) {
                     float m[W], v[W];
                     unit_moments<W, false>(s, grads, mc, vc,
-                                           base + int64_t(wk.row) * d.cols + wk.cu * W, ms_old,
+                                           base + int64_t(w1.row) * d.cols + w1.cu * W, ms_old,
                                            vs_old, m, v, mamax, vamax);
-                    wk.next();
+                    w1.next();
                 }
             }
         }
-        for (int o = lanes >> 1; o > 0; o >>= 1) {
+        for (int o = (lanes < 32 ? lanes : 32) >> 1; o > 0; o >>= 1) {
             mamax = fmaxf(mamax, __shfl_xor_sync(0xFFFFFFFFu, mamax, o));
             vamax = fmaxf(vamax, __shfl_xor_sync(0xFFFFFFFFu, vamax, o));
         }
+        if (lanes > 32) {
+            if ((tid & 31) == 0) red[par][tid >> 5] = make_float2(mamax, vamax);
+            __syncthreads();
+            const int w0 = (grp << sh) >> 5;
+            for (int q = 0; q < (lanes >> 5); ++q) {
+                const float2 r = red[par][w0 + q];
+                mamax = fmaxf(mamax, r.x);
+                vamax = fmaxf(vamax, r.y);
+            }
+        }
         if (!active) continue;
         const float ms_new = block_scale(mamax, 127.0f);
-        const float vs_new = __fdiv_rn(vamax, 256.0f);
+        const float vs_new = __fmul_rn(vamax, 0x1p-8f);  // = RN(vamax / 256), underflow included
         const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
         const bool vzero = !(vs_new > 0.0f);
         if (dm.exact || dv.exact)
-            pass2<W, true>(s, params, grads, mc, vc, base, d.cols, j, lanes, upr, nu, inreg, ms_old,
-                           vs_old, mr, vr, dm, dv, vzero);
+            pass2<W, true>(s, params, grads, mc, vc, base, d.cols, j, lanes, wk, nu, inreg, ms_old,
+                           vs_old, pr, mr, vr, dm, dv, vzero);
         else
-            pass2<W, false>(s, params, grads, mc, vc, base, d.cols, j, lanes, upr, nu, inreg,
-                            ms_old, vs_old, mr, vr, dm, dv, vzero);
+            pass2<W, false>(s, params, grads, mc, vc, base, d.cols, j, lanes, wk, nu, inreg,
+                            ms_old, vs_old, pr, mr, vr, dm, dv, vzero);
         if (j == 0) {
             ms[si] = ms_new;
             vs[si] = vs_new;
@@ -351,7 +481,9 @@ __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it
     }
 }
 
-__global__ void __launch_bounds__(kThreads)
+// Four CTAs per SM (64 registers): the step is bound by memory latency as much
+// as by instruction issue, and 32 warps per SM beat fewer, spill-free warps.
+__global__ void __launch_bounds__(kThreads, 4)
     adamw8_kernel(const Chunk *__restrict__ chunks, const int32_t *__restrict__ plain,
                   int32_t n_plain, const OptItem *__restrict__ items,
                   const TensorDesc *__restrict__ td, float *__restrict__ params,
@@ -359,13 +491,14 @@ __global__ void __launch_bounds__(kThreads)
                   uint8_t *__restrict__ vc, float *__restrict__ ms, float *__restrict__ vs,
                   float *__restrict__ m32, float *__restrict__ v32, const dbuf_adamw_hparams hp,
                   const float *__restrict__ total_norm, const int32_t *__restrict__ nonfinite) {
+    __shared__ float2 red[2][kThreads / 32];
     if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
     const AdamScalars s = adam_scalars(hp, total_norm);
     if (int(blockIdx.x) < n_plain) {
         const Chunk c = chunks[plain[blockIdx.x]];
         const int64_t base = td[c.tensor].buf_off + c.off;
         const int64_t sb = td[c.tensor].state_off + c.off;
-        adamw_range(s, params + base, grads + base, m32 + sb, v32 + sb, c.len);
+        adamw_range_lean(s, params + base, grads + base, m32 + sb, v32 + sb, c.len);
         return;
     }
     const OptItem it = items[blockIdx.x - n_plain];
@@ -374,9 +507,9 @@ __global__ void __launch_bounds__(kThreads)
                      aligned16(params, grads) &&
                      ((reinterpret_cast<uintptr_t>(mc) | reinterpret_cast<uintptr_t>(vc)) & 3) == 0;
     if (vec)
-        opt_item<4>(s, it, d, params, grads, mc, vc, ms, vs);
+        opt_item<4>(s, it, d, params, grads, mc, vc, ms, vs, red);
     else
-        opt_item<1>(s, it, d, params, grads, mc, vc, ms, vs);
+        opt_item<1>(s, it, d, params, grads, mc, vc, ms, vs, red);
 }
 
 }  // namespace

@@ -261,21 +261,22 @@ void build_tables(dbuf_plan_t *p) {
             const int64_t nbr = (s.rows + d.qrows - 1) / d.qrows;
             const int64_t nb = nbr * d.nbc;
             {
-                // 8-bit optimizer items: the fewest lanes per block that keep the
-                // block's moments in registers (units of 4 elements when rows and
-                // block widths allow vector access), 32 lanes and a recompute pass
-                // for larger blocks; about kOptItemElems elements per item.
+                // 8-bit optimizer items: the fewest threads per block that keep the
+                // block in registers (units of 4 elements when rows and block
+                // widths allow vector access), 256 threads and a recompute pass for
+                // larger blocks; about kOptItemElems elements per item.
                 const int64_t be = int64_t(d.qrows) * d.qcols;
                 const bool vec = d.qcols % 4 == 0 && s.cols % 4 == 0 && d.buf_off % 4 == 0;
                 const int64_t units = vec ? be / 4 : be;
                 int lanes = 4;
-                while (lanes < 32 && units > int64_t(lanes) * dbuf::kOptUnitsPerLane) lanes *= 2;
+                while (lanes < 256 && units > int64_t(lanes) * dbuf::kOptUnitsPerLane) lanes *= 2;
                 const int64_t groups = 256 / lanes;
                 int64_t per = std::max<int64_t>(1, dbuf::kOptItemElems / std::max<int64_t>(1, be));
                 per = std::max<int64_t>(groups, (per + groups - 1) / groups * groups);
                 per = std::min<int64_t>(per, 16384);
                 for (int64_t b = 0; b < nb; b += per)
-                    p->opt_items.push_back(dbuf::OptItem{b, t, int16_t(std::min(per, nb - b)),
+                    p->opt_items.push_back(dbuf::OptItem{t, int32_t(b / d.nbc), int32_t(b % d.nbc),
+                                                         int16_t(std::min(per, nb - b)),
                                                          int16_t(lanes)});
             }
             if (d.qrows == 1) {
