@@ -412,6 +412,30 @@ extern "C" int dbuf_plan_query(const dbuf_plan_t *p, int64_t *S, int64_t *total,
     return DBUF_OK;
 }
 
+extern "C" int dbuf_order(const dbuf_tensor_spec *specs, int32_t n, int32_t kind, int32_t *perm) {
+    if (n < 0 || (n > 0 && (!specs || !perm))) return DBUF_EINVAL;
+    if (kind != DBUF_ORDER_DEFAULT && kind != DBUF_ORDER_BLOCK && kind != DBUF_ORDER_SHAPE)
+        return DBUF_EINVAL;
+    std::vector<int32_t> idx(n);
+    for (int32_t t = 0; t < n; ++t) idx[t] = t;
+    auto unit = [&](int32_t t) {
+        const dbuf_tensor_spec &s = specs[t];
+        const int64_t numel = s.rows * s.cols;
+        const int64_t g = (s.gran_rows <= 0 || s.gran_rows >= s.rows) ? numel : s.gran_rows * s.cols;
+        return std::max<int64_t>(g, 1);
+    };
+    if (kind == DBUF_ORDER_BLOCK)
+        std::stable_sort(idx.begin(), idx.end(),
+                         [&](int32_t a, int32_t b) { return unit(a) > unit(b); });
+    else if (kind == DBUF_ORDER_SHAPE)
+        std::stable_sort(idx.begin(), idx.end(), [&](int32_t a, int32_t b) {
+            if (specs[a].rows != specs[b].rows) return specs[a].rows > specs[b].rows;
+            return specs[a].cols > specs[b].cols;
+        });
+    std::copy(idx.begin(), idx.end(), perm);
+    return DBUF_OK;
+}
+
 extern "C" int dbuf_plan_state_offsets(const dbuf_plan_t *p, int64_t *state_offsets,
                                        int64_t *n_state) {
     if (!p) return DBUF_EINVAL;

@@ -45,7 +45,7 @@ EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
            "dbuf_device_status", "dbuf_adamw_step", "dbuf_plan_state_offsets",
-           "dbuf_adamw8_step", "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_adamw8_step", "dbuf_order", "dbuf_strerror", "dbuf_last_cuda_error")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -117,6 +117,8 @@ def _lib_handle():
         L.dbuf_plan_state_offsets.restype = ctypes.c_int
         L.dbuf_adamw8_step.argtypes = [P, P, P, P, P, P, P, P, P, P, P, P, P]
         L.dbuf_adamw8_step.restype = ctypes.c_int
+        L.dbuf_order.argtypes = [P, i32, i32, P]
+        L.dbuf_order.restype = ctypes.c_int
         L.dbuf_device_status.argtypes = [P, P, P]
         L.dbuf_device_status.restype = ctypes.c_int
         L.dbuf_strerror.argtypes = [ctypes.c_int]
@@ -160,6 +162,18 @@ def dbuf_plan(specs: Sequence, m: int, local_units: Optional[Sequence[int]] = No
     _check(_lib_handle().dbuf_plan(arr, len(specs), m, units, align_elems, ctypes.byref(out)),
            "dbuf_plan")
     return out.value
+
+
+DBUF_ORDER = {"default": 0, "block": 1, "shape": 2}
+
+
+def dbuf_order(specs, kind: str = "default") -> list:
+    """Placement permutation of the specs for one of the studied orders:
+    perm[i] is the index of the tensor placed i-th."""
+    arr = _spec_array(specs)
+    perm = (ctypes.c_int32 * max(len(specs), 1))()
+    _check(_lib_handle().dbuf_order(arr, len(specs), DBUF_ORDER[kind], perm), "dbuf_order")
+    return list(perm)[:len(specs)]
 
 
 def dbuf_plan_query(plan: int, n: int, m: int) -> dict:

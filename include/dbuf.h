@@ -128,6 +128,27 @@ typedef struct dbuf_plan dbuf_plan_t;
 int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
               const int32_t *local_units, int64_t align_elems, dbuf_plan_t **out);
 
+/* Tensor orders for dbuf_order. */
+#define DBUF_ORDER_DEFAULT 0 /* as given (the order the pages adopt) */
+#define DBUF_ORDER_BLOCK 1   /* by block size: g_t descending */
+#define DBUF_ORDER_SHAPE 2   /* by shape: (rows, cols) descending */
+
+/*
+ * dbuf_order -- host only, no CUDA call.  The placement orders the planner
+ * was studied with [veScale-FSDP §5: default order, block-size order and
+ * tensor-shape order were compared; the default order was optimal or nearly
+ * so and is the one adopted].  The pages name the orders but not their
+ * direction or tie-break; this library reads them as stable sorts, largest
+ * first, ties kept in the given order:
+ *   DBUF_ORDER_BLOCK  key g_t, the elements of one shard unit (gran_rows * cols,
+ *                     or numel when gran_rows is 0 or >= rows; at least 1);
+ *   DBUF_ORDER_SHAPE  key (rows, cols), compared lexicographically.
+ * perm: host array of n; perm[i] receives the index (in specs) of the tensor
+ * placed i-th.  To plan in that order, pass the permuted specs to dbuf_plan.
+ * Errors: DBUF_EINVAL (specs or perm NULL with n > 0, n < 0, unknown kind).
+ */
+int dbuf_order(const dbuf_tensor_spec *specs, int32_t n, int32_t kind, int32_t *perm);
+
 /*
  * dbuf_plan_query -- host only.  Copies the plan's results into host arrays;
  * any output pointer may be NULL.

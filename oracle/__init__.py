@@ -299,3 +299,29 @@ def adamw8(p: Plan, specs, params: np.ndarray, grad: np.ndarray, m_codes: np.nda
                      _p(grad), _p(m_codes), _p(v_codes), _p(m_scales), _p(v_scales), _p(m32),
                      _p(v32), lr, beta1, beta2, eps, weight_decay, bc1, bc2, max_norm,
                      total_norm, int(nonfinite))
+
+
+# ----------------------------------------------------------------------------
+# placement orders
+# ----------------------------------------------------------------------------
+
+def shard_unit(spec) -> int:
+    """g_t: elements of one shard unit (whole tensor when gran_rows is 0 or
+    covers every row), at least 1."""
+    numel = spec.rows * spec.cols
+    g = numel if (spec.gran_rows <= 0 or spec.gran_rows >= spec.rows) else spec.gran_rows * spec.cols
+    return max(g, 1)
+
+
+def order(specs, kind: str = "default") -> List[int]:
+    """The tensor orders the planner was studied with [veScale-FSDP, §5 Planning
+    algorithm: default order, block-size order, tensor-shape order].  Read as
+    stable sorts, largest first: block size = g_t, shape = (rows, cols)."""
+    idx = list(range(len(specs)))
+    if kind == "default":
+        return idx
+    if kind == "block":
+        return sorted(idx, key=lambda t: -shard_unit(specs[t]))
+    if kind == "shape":
+        return sorted(idx, key=lambda t: (-specs[t].rows, -specs[t].cols))
+    raise ValueError(kind)
