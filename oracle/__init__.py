@@ -89,6 +89,9 @@ def lib():
         L.orc_adamw8.argtypes = [i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
                                  f, f, f, f, f, f, f, f, f, i32]
         L.orc_adamw8.restype = None
+        for fn in ("orc_gather", "orc_scatter"):
+            getattr(L, fn).argtypes = [i32, P, P, i32, P, P, i32, P]
+            getattr(L, fn).restype = None
         _lib = L
     return _lib
 
@@ -325,3 +328,27 @@ def order(specs, kind: str = "default") -> List[int]:
     if kind == "shape":
         return sorted(idx, key=lambda t: (-specs[t].rows, -specs[t].cols))
     raise ValueError(kind)
+
+
+# ----------------------------------------------------------------------------
+# whole-matrix gather / scatter (Muon-style updates)
+# ----------------------------------------------------------------------------
+
+def _ptr_array(arrs):
+    return (ctypes.c_void_p * max(len(arrs), 1))(
+        *[(a.ctypes.data if a is not None else None) for a in arrs])
+
+
+def gather(p: Plan, shards: List[np.ndarray], dsts: List[Optional[np.ndarray]]) -> None:
+    """dsts[t] <- tensor t assembled from the m shard buffers (None = skip)."""
+    dt = _dt(shards[0])
+    assert len(shards) == len(p.bounds) - 1
+    lib().orc_gather(len(p.offsets), _p(p.offsets), _p(_i64(p.numel)), len(shards),
+                     _p(p.bounds), _ptr_array(shards), dt, _ptr_array(dsts))
+
+
+def scatter(p: Plan, srcs: List[Optional[np.ndarray]], shards: List[np.ndarray]) -> None:
+    """Tensor t's elements from srcs[t] back into the m shard buffers (None = skip)."""
+    dt = _dt(shards[0])
+    lib().orc_scatter(len(p.offsets), _p(p.offsets), _p(_i64(p.numel)), len(shards),
+                      _p(p.bounds), _ptr_array(srcs), dt, _ptr_array(shards))

@@ -600,3 +600,52 @@ void orc_adamw8(int32_t n, const int64_t *offsets, const int64_t *rows, const in
         s_off += nbr * nbc;
     }
 }
+
+/* Shard holding flat position pos: the k with bounds[k] <= pos < bounds[k+1]. */
+static int32_t shard_of(int32_t m, const int64_t *bounds, int64_t pos)
+{
+    int32_t k = 0;
+    while (k + 1 < m && bounds[k + 1] <= pos) ++k;
+    return k;
+}
+
+/* Whole-matrix gather for Muon-style updates [veScale-FSDP, §6.3 Distributed
+ * Muon: each matrix is redistributed to a root as the full 2-D matrix, updated
+ * there, and the update redistributed back (Algorithm 2)].  The m shards are
+ * separate buffers: shard k holds flat positions [bounds[k], bounds[k+1]) at
+ * local offsets 0..; element i of tensor t (flat position offsets[t] + i) is
+ * copied to dst[t][i].  Tensors with dst[t] == NULL are skipped.  Elements are
+ * moved as raw bytes of the dtype (no conversion). */
+void orc_gather(int32_t n, const int64_t *offsets, const int64_t *numel, int32_t m,
+                const int64_t *bounds, void *const *shards, int32_t dtype, void *const *dst)
+{
+    size_t es = dtype == ORC_BF16 ? 2 : 4;
+    for (int32_t t = 0; t < n; ++t) {
+        if (!dst[t]) continue;
+        for (int64_t i = 0; i < numel[t]; ++i) {
+            int64_t pos = offsets[t] + i;
+            int32_t k = shard_of(m, bounds, pos);
+            memcpy((char *)dst[t] + (size_t)i * es,
+                   (const char *)shards[k] + (size_t)(pos - bounds[k]) * es, es);
+        }
+    }
+}
+
+/* The way back: element i of src[t] goes to its shard position.  Tensors with
+ * src[t] == NULL are left as they are; shard bytes outside tensor ranges are
+ * never written. */
+void orc_scatter(int32_t n, const int64_t *offsets, const int64_t *numel, int32_t m,
+                 const int64_t *bounds, const void *const *src, int32_t dtype,
+                 void *const *shards)
+{
+    size_t es = dtype == ORC_BF16 ? 2 : 4;
+    for (int32_t t = 0; t < n; ++t) {
+        if (!src[t]) continue;
+        for (int64_t i = 0; i < numel[t]; ++i) {
+            int64_t pos = offsets[t] + i;
+            int32_t k = shard_of(m, bounds, pos);
+            memcpy((char *)shards[k] + (size_t)(pos - bounds[k]) * es,
+                   (const char *)src[t] + (size_t)i * es, es);
+        }
+    }
+}
