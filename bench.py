@@ -550,6 +550,7 @@ def run_ours(args):
     # ---- the next row: fused AdamW step over every DBuffer (separate timing)
     adamw = None if args.no_adamw else run_adamw(stack, args, world, peak, barrier)
     adamw8 = None if args.no_adamw else run_adamw8(stack, args, world, peak, barrier)
+    gather = None if args.no_adamw else run_gather(stack, args, world, peak, barrier)
 
     # ---- end to end: host inputs (pinned) -> device, operators, results -> host
     e2e = None if args.no_e2e else run_e2e(stack, args, world)
@@ -575,7 +576,8 @@ def run_ours(args):
                 "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": stack.launches_per_step * args.steps,
-                "next_rows": ({"adamw": adamw, "adamw8": adamw8} if adamw else None),
+                "next_rows": ({"adamw": adamw, "adamw8": adamw8, "gather_scatter": gather}
+                              if adamw else None),
                 "launch": "eager" if args.eager else "cuda_graph (K steps captured once, replayed)",
                 "ops_note": ("per-operator times from one step with events around every "
                              "operator, outside the timed region" +
@@ -717,6 +719,59 @@ def run_adamw8(stack, args, world, peak, barrier):
             "frac_of_peak": round(gbs / world / peak, 4),
             "bytes_per_step": nbytes, "flat_elements_per_step": elems,
             "launches_per_step": len(order)}
+
+
+def run_gather(stack, args, world, peak, barrier):
+    """Whole-matrix gather and scatter (dbuf_gather + dbuf_scatter) of every
+    tensor of every DBuffer: the m shards are the slices [B_k, B_{k+1}) of the
+    group's fp32 accumulator, the matrices separate fp32 buffers.  One gather
+    and one scatter per DBuffer per step; K steps captured once as a CUDA graph
+    and timed as one replay.  Algorithmic bytes: 16 per element (each copy
+    reads and writes 4)."""
+    device = stack.device
+    for d in stack.dbufs:
+        k = d["kind"]
+        if "mats" not in k:
+            db = k["db"]
+            b = db.shard_bounds
+            k["shards"] = [k["acc"][b[i]:b[i + 1]] for i in range(db.m)]
+            k["mats"] = [torch.empty(s.numel, dtype=torch.float32, device=device)
+                         for s in k["spec"].tensors]
+
+    def step():
+        for d in stack.dbufs:
+            k = d["kind"]
+            k["db"].gather(k["shards"], k["mats"])
+            k["db"].scatter(k["mats"], k["shards"])
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    graph = None
+    if not args.eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for _ in range(args.steps):
+                step()
+        graph.replay()
+        torch.cuda.synchronize()
+    barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    if graph is not None:
+        graph.replay()
+    else:
+        for _ in range(args.steps):
+            step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(s.elapsed_time(e), device) / args.steps
+    nbytes = 16 * stack.elements
+    gbs = job_throughput(nbytes, ms, world)
+    return {"op": "dbuf_gather + dbuf_scatter (every tensor, fp32, m shard slices)",
+            "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),
+            "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 16,
+            "launches_per_step": 2 * len(stack.dbufs)}
 
 
 def run_e2e(stack, args, world):

@@ -52,7 +52,8 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     const size_t b_p = align256(sizeof(dbuf::TileItem) * p->pipe_items.size());
     const size_t b_o = align256(sizeof(dbuf::OptItem) * p->opt_items.size());
     const size_t b_a = align256(sizeof(int32_t) * p->opt_plain.size());
-    const size_t bytes = b_t + b_c + b_r + b_q + b_p + b_o + b_a + 256;
+    const size_t b_g = align256(sizeof(dbuf::Piece) * p->pieces.size());
+    const size_t bytes = b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g + 256;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -76,7 +77,8 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     t.pipe_items = reinterpret_cast<dbuf::TileItem *>(c + b_t + b_c + b_r + b_q);
     t.opt_items = reinterpret_cast<dbuf::OptItem *>(c + b_t + b_c + b_r + b_q + b_p);
     t.opt_plain = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o);
-    t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a);
+    t.pieces = reinterpret_cast<dbuf::Piece *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a);
+    t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g);
     t.num_sms = sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = cudaMemsetAsync(t.status, 0, sizeof(int32_t), st);
@@ -88,7 +90,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
         void *dst;
         const void *src;
         size_t n;
-    } pieces[7] = {
+    } pieces[8] = {
         {t.tensors, p->tdesc.data(), sizeof(dbuf::TensorDesc) * p->tdesc.size()},
         {t.chunks, p->chunks.data(), sizeof(dbuf::Chunk) * p->chunks.size()},
         {t.row_items, p->row_items.data(), sizeof(dbuf::RowItem) * p->row_items.size()},
@@ -96,6 +98,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
         {t.pipe_items, p->pipe_items.data(), sizeof(dbuf::TileItem) * p->pipe_items.size()},
         {t.opt_items, p->opt_items.data(), sizeof(dbuf::OptItem) * p->opt_items.size()},
         {t.opt_plain, p->opt_plain.data(), sizeof(int32_t) * p->opt_plain.size()},
+        {t.pieces, p->pieces.data(), sizeof(dbuf::Piece) * p->pieces.size()},
     };
     for (const Piece &pc : pieces) {
         if (!pc.n) continue;
@@ -224,4 +227,22 @@ extern "C" int dbuf_adamw8_step(const dbuf_plan_t *p, float *params, const float
     return finish(dbuf::launch_adamw8(p, params, grads, exp_avg_codes, exp_avg_sq_codes,
                                       exp_avg_scales, exp_avg_sq_scales, exp_avg_fp32,
                                       exp_avg_sq_fp32, *hp, total_norm, nonfinite, stream));
+}
+
+extern "C" int dbuf_gather(const dbuf_plan_t *p, void *const *shards, int32_t dtype,
+                           void *const *dst, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(dtype)) return DBUF_EINVAL;
+    if (p->n > 0 && (!shards || !dst)) return DBUF_EINVAL;
+    return finish(dbuf::launch_gather(p, shards, dtype, dst, stream));
+}
+
+extern "C" int dbuf_scatter(const dbuf_plan_t *p, const void *const *src, int32_t dtype,
+                            void *const *shards, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(dtype)) return DBUF_EINVAL;
+    if (p->n > 0 && (!shards || !src)) return DBUF_EINVAL;
+    return finish(dbuf::launch_scatter(p, src, dtype, shards, stream));
 }

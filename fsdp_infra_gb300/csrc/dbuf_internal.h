@@ -86,6 +86,19 @@ struct OptItem {
 };
 static_assert(sizeof(OptItem) == 16, "OptItem layout");
 
+// A piece of one tensor inside one shard, for the whole-matrix gather and
+// scatter: elements [off, off+len) of tensor `tensor` sit at [shard_off,
+// shard_off+len) of shard `shard`.  Pieces are chunks split at shard bounds.
+struct Piece {
+    int64_t off;
+    int64_t shard_off;
+    int32_t tensor;
+    int32_t len;
+    int32_t shard;
+    int32_t reserved;
+};
+static_assert(sizeof(Piece) == 32, "Piece layout");
+
 // Moment units (4 elements on the vector path) that one thread of the 8-bit
 // optimizer keeps in registers; larger blocks are recomputed in a second pass.
 constexpr int kOptUnitsPerLane = 2;
@@ -104,6 +117,7 @@ struct DeviceTables {
     TileItem *pipe_items = nullptr;  // tiles for the pipelined kernel
     OptItem *opt_items = nullptr;    // 8-bit optimizer: blocks of quantised tensors
     int32_t *opt_plain = nullptr;    // 8-bit optimizer: chunks of the other tensors
+    Piece *pieces = nullptr;         // gather / scatter: chunks split at shard bounds
     int32_t *status = nullptr;       // device status word (0, or DBUF_ETIMEOUT)
     void *base = nullptr;
     size_t bytes = 0;
@@ -132,6 +146,11 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
                   uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
                   const dbuf_adamw_hparams &hp, const float *total_norm, const int32_t *nonfinite,
                   void *stream);
+
+int launch_gather(const dbuf_plan_t *p, void *const *shards, int dt, void *const *dst,
+                  void *stream);
+int launch_scatter(const dbuf_plan_t *p, const void *const *src, int dt, void *const *shards,
+                   void *stream);
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p);
 
@@ -167,6 +186,7 @@ struct dbuf_plan {
     std::vector<int32_t> pipe_tensors;  // slot -> tensor id
     std::vector<dbuf::OptItem> opt_items;
     std::vector<int32_t> opt_plain;      // chunk ids of tensors without quantisation
+    std::vector<dbuf::Piece> pieces;
     std::vector<int64_t> state_offsets;  // [n], -1 for quantised tensors
     int64_t n_state = 0;
 

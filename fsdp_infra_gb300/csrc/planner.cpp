@@ -308,6 +308,22 @@ void build_tables(dbuf_plan_t *p) {
     }
     p->n_scales = s_off;
     p->n_state = st_off;
+
+    // gather / scatter pieces: each tensor's chunks cut again at shard bounds
+    p->pieces.clear();
+    int32_t k = 0;
+    for (int32_t t = 0; t < n; ++t) {
+        const int64_t l = p->offsets[t], numel = p->tdesc[t].numel;
+        int64_t i = 0;
+        while (i < numel) {
+            const int64_t pos = l + i;
+            while (k + 1 < p->m && p->bounds[k + 1] <= pos) ++k;
+            int64_t end = std::min(numel, (i / dbuf::kChunkElems + 1) * dbuf::kChunkElems);
+            end = std::min(end, p->bounds[k + 1] - l);
+            p->pieces.push_back(dbuf::Piece{i, pos - p->bounds[k], t, int32_t(end - i), k, 0});
+            i = end;
+        }
+    }
 }
 
 }  // namespace
@@ -386,7 +402,8 @@ extern "C" int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
         build_tables(p);
         if (p->chunks.size() > size_t(INT32_MAX) || p->tile_items.size() > size_t(INT32_MAX) ||
             p->row_items.size() > size_t(INT32_MAX) || p->pipe_items.size() > size_t(INT32_MAX) ||
-            p->opt_items.size() + p->opt_plain.size() > size_t(INT32_MAX)) {
+            p->opt_items.size() + p->opt_plain.size() > size_t(INT32_MAX) ||
+            p->pieces.size() > size_t(INT32_MAX)) {
             delete p;
             return DBUF_ERANGE;
         }

@@ -45,7 +45,8 @@ EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
            "dbuf_device_status", "dbuf_adamw_step", "dbuf_plan_state_offsets",
-           "dbuf_adamw8_step", "dbuf_order", "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_adamw8_step", "dbuf_order", "dbuf_gather", "dbuf_scatter", "dbuf_strerror",
+           "dbuf_last_cuda_error")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -119,6 +120,9 @@ def _lib_handle():
         L.dbuf_adamw8_step.restype = ctypes.c_int
         L.dbuf_order.argtypes = [P, i32, i32, P]
         L.dbuf_order.restype = ctypes.c_int
+        for fn in ("dbuf_gather", "dbuf_scatter"):
+            getattr(L, fn).argtypes = [P, P, i32, P, P]
+            getattr(L, fn).restype = ctypes.c_int
         L.dbuf_device_status.argtypes = [P, P, P]
         L.dbuf_device_status.restype = ctypes.c_int
         L.dbuf_strerror.argtypes = [ctypes.c_int]
@@ -276,6 +280,14 @@ def dbuf_adamw8_step(plan: int, params: int, grads: int, exp_avg_codes: int,
                                           exp_avg_sq_fp32 or None, ctypes.byref(hp),
                                           total_norm or None, nonfinite or None, stream),
            "dbuf_adamw8_step")
+
+
+def dbuf_gather(plan: int, shard_ptrs: int, dtype: int, dst_ptrs: int, stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_gather(plan, shard_ptrs, dtype, dst_ptrs, stream), "dbuf_gather")
+
+
+def dbuf_scatter(plan: int, src_ptrs: int, dtype: int, shard_ptrs: int, stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_scatter(plan, src_ptrs, dtype, shard_ptrs, stream), "dbuf_scatter")
 
 
 def dbuf_device_status(plan: int, stream: int = 0) -> int:

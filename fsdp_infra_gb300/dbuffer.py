@@ -235,3 +235,55 @@ class DBuffer:
                             nonfinite=nonfinite.data_ptr() if nonfinite is not None else 0,
                             stream=self._stream(stream))
 
+    # -- whole-matrix gather / scatter -------------------------------------------
+    def shard_sizes(self) -> List[int]:
+        """Elements of each of the m shard slices (B_{k+1} - B_k)."""
+        b = self.shard_bounds
+        return [b[k + 1] - b[k] for k in range(self.m)]
+
+    def _opt_ptr_table(self, tensors, numels, what) -> torch.Tensor:
+        """Device array of data pointers (0 for None), cached per tuple of
+        (pointer, element count, dtype) like ptr_table."""
+        key = (what,) + tuple(None if x is None else (x.data_ptr(), x.numel(), x.dtype)
+                              for x in tensors)
+        tab = self._ptr_tables.get(key)
+        if tab is not None:
+            return tab
+        ptrs = []
+        for t, x in enumerate(tensors):
+            if x is None:
+                ptrs.append(0)
+                continue
+            if not x.is_contiguous() or x.numel() != numels[t] or x.device != self.device:
+                raise ValueError(f"{what} {t}: want a contiguous tensor of {numels[t]} "
+                                 f"elements on {self.device}")
+            ptrs.append(x.data_ptr())
+        tab = torch.tensor(ptrs or [0], dtype=torch.int64, device=self.device)
+        self._ptr_tables[key] = tab
+        return tab
+
+    def gather(self, shards: Sequence[torch.Tensor], dsts: Sequence[Optional[torch.Tensor]],
+               stream=None) -> None:
+        """dsts[t] <- tensor t's full matrix assembled from the m shard buffers
+        (None skips the tensor)."""
+        if len(shards) != self.m or len(dsts) != self.n:
+            raise ValueError("gather wants m shards and n destinations")
+        dt = dtype_code(shards[0].dtype)
+        if any(x is not None and x.dtype != shards[0].dtype for x in list(shards) + list(dsts)):
+            raise TypeError("shards and matrices must share one dtype")
+        sh = self._opt_ptr_table(shards, self.shard_sizes(), "shard")
+        tab = self._opt_ptr_table(dsts, self.numel, "matrix")
+        _c.dbuf_gather(self.handle, sh.data_ptr(), dt, tab.data_ptr(), self._stream(stream))
+
+    def scatter(self, srcs: Sequence[Optional[torch.Tensor]], shards: Sequence[torch.Tensor],
+                stream=None) -> None:
+        """Tensor t's full matrix srcs[t] back into the m shard buffers (None skips)."""
+        if len(shards) != self.m or len(srcs) != self.n:
+            raise ValueError("scatter wants n sources and m shards")
+        dt = dtype_code(shards[0].dtype)
+        if any(x is not None and x.dtype != shards[0].dtype for x in list(shards) + list(srcs)):
+            raise TypeError("shards and matrices must share one dtype")
+        sh = self._opt_ptr_table(shards, self.shard_sizes(), "shard")
+        tab = self._opt_ptr_table(srcs, self.numel, "matrix")
+        _c.dbuf_scatter(self.handle, tab.data_ptr(), dt, sh.data_ptr(), self._stream(stream))
+

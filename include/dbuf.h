@@ -397,6 +397,35 @@ int dbuf_adamw8_step(const dbuf_plan_t *plan, float *params, const float *grads,
                      const dbuf_adamw_hparams *hp, const float *total_norm,
                      const int32_t *nonfinite, void *stream);
 
+/*
+ * dbuf_gather -- whole-matrix gather: assembles tensors, each as its full
+ * row-major matrix, from the m shard buffers, one launch.  [veScale-FSDP §6.3
+ * Distributed Muon: a matrix-sign preconditioner needs the whole 2-D matrix,
+ * so each matrix is redistributed to a root, updated there, and the update
+ * redistributed back (Algorithm 2).  On one GPU the redistribution is this
+ * copy; the update itself is the caller's.]
+ *   shards: device array of m device pointers; shard k holds the plan's flat
+ *           positions [B_k, B_{k+1}) at its local offsets 0.. (e.g. each
+ *           rank's local shard buffer); every pointer must be valid.
+ *   dtype:  DBUF_F32 or DBUF_BF16 for both sides (bytes are copied unchanged).
+ *   dst:    device array of n device pointers; dst[t] receives the numel_t
+ *           elements of tensor t; a NULL entry skips the tensor.
+ * Padding bytes of the shards are never read.  16-byte aligned ends take the
+ * vector path.  Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE,
+ * DBUF_ECUDA.
+ */
+int dbuf_gather(const dbuf_plan_t *plan, void *const *shards, int32_t dtype, void *const *dst,
+                void *stream);
+
+/*
+ * dbuf_scatter -- the way back of dbuf_gather: src[t] (device pointer to the
+ * full matrix of tensor t, NULL to skip) is written to the tensor's positions
+ * in the m shard buffers.  Shard padding is never written.  Arguments and
+ * errors as for dbuf_gather.
+ */
+int dbuf_scatter(const dbuf_plan_t *plan, const void *const *src, int32_t dtype,
+                 void *const *shards, void *stream);
+
 /* dbuf_strerror -- static description of a return code. */
 const char *dbuf_strerror(int code);
 
