@@ -36,6 +36,9 @@ constexpr int kUnroll = 2;
 
 struct AdamScalars {
     float coef, decay, step, beta1, beta2, omb1, omb2, bc2, eps;
+    float ibc2;  // RN(1 / bc2), for the 8-bit step's quotient
+    float i127;  // RN(1 / 127), for the 8-bit step's block scale
+    bool fast;   // bc2 and eps inside the range of the correctly rounded forms
 };
 
 __device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp,
@@ -54,6 +57,9 @@ __device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp
     s.omb2 = __fsub_rn(1.0f, hp.beta2);
     s.bc2 = hp.bias_correction2;
     s.eps = hp.eps;
+    s.ibc2 = __frcp_rn(s.bc2);
+    s.i127 = __frcp_rn(127.0f);
+    s.fast = s.bc2 >= 0x1p-40f && s.bc2 <= 1.0f && s.eps >= 0.0f && s.eps <= 0x1p40f;
     return s;
 }
 
@@ -69,6 +75,15 @@ __device__ __forceinline__ float adam_param(const AdamScalars &s, float p, float
     const float pd = __fmul_rn(p, s.decay);
     const float denom = __fadd_rn(__fsqrt_rn(__fdiv_rn(v, s.bc2)), s.eps);
     return __fsub_rn(pd, __fmul_rn(s.step, __fdiv_rn(m, denom)));
+}
+
+// adam_param with the correctly rounded forms; equal to it whenever |m| and v
+// lie in [2^-60, 2^60] and s.fast holds: v/bc2 is then in [2^-60, 2^100], its
+// square root plus eps in [2^-30, 2^51], and m over that in the normal range.
+__device__ __forceinline__ float adam_param_cr(const AdamScalars &s, float p, float m, float v) {
+    const float pd = __fmul_rn(p, s.decay);
+    const float denom = __fadd_rn(sqrt_cr(div_cr(v, s.bc2, s.ibc2)), s.eps);
+    return __fsub_rn(pd, __fmul_rn(s.step, div_cr(m, denom, rcp_cr(denom))));
 }
 
 __device__ __forceinline__ void adam_elem(const AdamScalars &s, float &p, float g, float &m,
@@ -203,6 +218,22 @@ __device__ __forceinline__ uint32_t low_bytes(float a, float b, float c, float d
     return __byte_perm(ab, cd, 0x5410u);
 }
 
+// Whether pass 1 also loads the parameters of an in-register block (one memory
+// latency per round, more registers) or pass 2 does.
+constexpr bool kLoadParamsEarly = true;
+
+// Whether dequantisation and encoding use packed fp32x2 operations (half the
+// floating-point instructions, but operands in aligned register pairs) or
+// scalar ones.
+constexpr bool kPackedCodes = true;
+
+// x / d.s for a scale inside the reciprocal step's range, without the sign
+// fix-up (a zero quotient's sign does not change an 8-bit code).
+__device__ __forceinline__ float quot_nosign(float x, const Divisor &d) {
+    const float q = __fmul_rn(x, d.y);
+    return __fmaf_rn(__fmaf_rn(-q, d.s, x), d.y, q);
+}
+
 // A lane's unit is W consecutive elements of one block row (W = 4 on the
 // vector path).  STREAM marks loads of data read once (evict-first).
 template <int W, bool STREAM>
@@ -252,7 +283,17 @@ __device__ __forceinline__ void unit_moments(const AdamScalars &s, const float *
     float g[W];
     load_f<W, STREAM>(grads, e, g);
     const uint32_t cm = load_c<W, STREAM>(mc, e), cv = load_c<W, STREAM>(vc, e);
-    if constexpr (W == 4) {
+    if constexpr (W == 4 && !kPackedCodes) {
+        const uint32_t xm = cm ^ 0x80808080u;
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            m[w] = __fmul_rn(__fadd_rn(byte_float(xm, w), -8388736.0f), ms_old);
+            v[w] = __fmul_rn(__fadd_rn(byte_float(cv, w), -8388607.0f), vs_old);
+            adam_moments(s, g[w], m[w], v[w]);
+            mamax = fmaxf(mamax, fabsf(m[w]));
+            vamax = fmaxf(vamax, v[w]);
+        }
+    } else if constexpr (W == 4) {
         // int8 c: the byte c ^ 0x80 = c + 128, so c = (2^23 + c + 128) - (2^23 + 128)
         const uint32_t xm = cm ^ 0x80808080u;
         const float2 om = splat(-8388736.0f), ov = splat(-8388607.0f);
@@ -293,13 +334,32 @@ template <int W, bool EXACT>
 __device__ __forceinline__ void unit_update(const AdamScalars &s, float *params, uint8_t *mc,
                                             uint8_t *vc, int64_t e, const float (&pin)[W],
                                             const float (&m)[W], const float (&v)[W],
-                                            const Divisor &dm, const Divisor &dv, bool vzero) {
+                                            const Divisor &dm, const Divisor &dv, bool vzero,
+                                            bool fast) {
     float p[W];
     uint32_t cm = 0, cv = 0;
     if constexpr (W == 4) {
+        bool cr = fast;
 #pragma unroll
-        for (int w = 0; w < 4; ++w) p[w] = adam_param(s, pin[w], m[w], v[w]);
-        if (!EXACT) {
+        for (int w = 0; w < 4; ++w) cr = cr && v[w] >= 0x1p-60f && fabsf(m[w]) >= 0x1p-60f;
+        if (cr) {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) p[w] = adam_param_cr(s, pin[w], m[w], v[w]);
+        } else {
+#pragma unroll
+            for (int w = 0; w < 4; ++w) p[w] = adam_param(s, pin[w], m[w], v[w]);
+        }
+        if (!EXACT && !kPackedCodes) {
+            float qm[4], qv[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                qm[w] = __fadd_rn(quot_nosign(m[w], dm), kMagicRound);
+                qv[w] = __fadd_rn(__fadd_rn(fmaxf(quot_nosign(v[w], dv), 1.0f), kMagicRound),
+                                  -1.0f);
+            }
+            cm = low_bytes(qm[0], qm[1], qm[2], qm[3]);
+            cv = low_bytes(qv[0], qv[1], qv[2], qv[3]);
+        } else if (!EXACT) {
             const float2 mg = splat(kMagicRound);
             const float2 qm01 = __fadd2_rn(quot2(make_float2(m[0], m[1]), dm), mg);
             const float2 qm23 = __fadd2_rn(quot2(make_float2(m[2], m[3]), dm), mg);
@@ -348,22 +408,65 @@ struct UnitWalk {
     }
 };
 
+// The same walk as a 32-bit element offset from the block's first element:
+// each step adds dr rows and dc units, and a wrap moves to the next row.  Used
+// for blocks whose offsets stay below 2^31 (qrows * cols < 2^31).
+template <int W>
+struct Walk32 {
+    int cu, dc, upr;
+    unsigned off, step, wrap;  // unsigned: steps past the block's last unit wrap harmlessly
+    __device__ __forceinline__ Walk32(int j, int lanes, int upr_, int cols) : upr(upr_) {
+        const int row = j / upr;
+        cu = j - row * upr;
+        off = unsigned(row) * unsigned(cols) + unsigned(cu * W);
+        const int dr = lanes / upr;
+        dc = lanes - dr * upr;
+        step = unsigned(dr) * unsigned(cols) + unsigned(dc * W);
+        wrap = unsigned(cols) - unsigned(upr * W);
+    }
+    __device__ __forceinline__ void next() {
+        cu += dc;
+        off += step;
+        if (cu >= upr) {
+            cu -= upr;
+            off += wrap;
+        }
+    }
+};
+
 template <int W, bool EXACT>
 __device__ __forceinline__ void pass2(const AdamScalars &s, float *params, const float *grads,
                                       uint8_t *mc, uint8_t *vc, int64_t base, int64_t cols,
-                                      int j, int lanes, UnitWalk wk, int nu, bool inreg,
-                                      float ms_old, float vs_old,
+                                      int j, int lanes, UnitWalk wk, Walk32<W> w32, int nu,
+                                      bool inreg, float ms_old, float vs_old,
                                       const float (&pr)[kOptUnitsPerLane][W],
                                       const float (&mr)[kOptUnitsPerLane][W],
                                       const float (&vr)[kOptUnitsPerLane][W], const Divisor &dm,
-                                      const Divisor &dv, bool vzero) {
+                                      const Divisor &dv, bool vzero, bool fast) {
     if (inreg) {
+        float *pb = params + base;
+        uint8_t *mb = mc + base;
+        uint8_t *vb = vc + base;
+        float pl[kOptUnitsPerLane][W];
+        if (!kLoadParamsEarly) {
+            Walk32<W> w0 = w32;
+#pragma unroll
+            for (int i = 0; i < kOptUnitsPerLane; ++i) {
+                if (j + i * lanes < nu) load_f<W, true>(pb, w0.off, pl[i]);
+                w0.next();
+            }
+        }
 #pragma unroll
         for (int i = 0; i < kOptUnitsPerLane; ++i) {
-            if (j + i * lanes < nu)
-                unit_update<W, EXACT>(s, params, mc, vc, base + int64_t(wk.row) * cols + wk.cu * W,
-                                      pr[i], mr[i], vr[i], dm, dv, vzero);
-            wk.next();
+            if (j + i * lanes < nu) {
+                if constexpr (kLoadParamsEarly)
+                    unit_update<W, EXACT>(s, pb, mb, vb, w32.off, pr[i], mr[i], vr[i], dm, dv,
+                                          vzero, fast);
+                else
+                    unit_update<W, EXACT>(s, pb, mb, vb, w32.off, pl[i], mr[i], vr[i], dm, dv,
+                                          vzero, fast);
+            }
+            w32.next();
         }
     } else {
         for (int u = j; u < nu; u += lanes) {
@@ -371,7 +474,7 @@ __device__ __forceinline__ void pass2(const AdamScalars &s, float *params, const
             float p[W], m[W], v[W], ma = 0.0f, va = 0.0f;
             load_f<W, true>(params, e, p);
             unit_moments<W, false>(s, grads, mc, vc, e, ms_old, vs_old, m, v, ma, va);
-            unit_update<W, EXACT>(s, params, mc, vc, e, p, m, v, dm, dv, vzero);
+            unit_update<W, EXACT>(s, params, mc, vc, e, p, m, v, dm, dv, vzero, fast);
             wk.next();
         }
     }
@@ -394,8 +497,15 @@ __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it
     const int tid = int(threadIdx.x);
     const int grp = tid >> sh, j = tid & (lanes - 1);
     const int nbc = d.nbc;
+    // the lanes of this thread's group within its warp (the whole warp when the
+    // group spans warps)
+    const unsigned gmask = lanes >= 32 ? 0xFFFFFFFFu
+                                       : ((1u << lanes) - 1u) << ((tid & 31) & ~(lanes - 1));
     // the walk over a full-width block, shared by all but the right-edge blocks
     const UnitWalk wfull(j, lanes, d.qcols / W);
+    // 32-bit offsets inside a block when its rows span less than 2^31 elements
+    const bool small = int64_t(d.qrows) * d.cols < (int64_t(1) << 31);
+    const Walk32<W> w32full(j, lanes, d.qcols / W, small ? int(d.cols) : 0);
     int par = 0;
     for (int k0 = 0; k0 < it.count; k0 += groups, par ^= 1) {
         const int k = k0 + grp;
@@ -404,6 +514,7 @@ __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it
         int upr = 1, nu = 0;
         float ms_old = 0.0f, vs_old = 0.0f;
         UnitWalk wk = wfull;
+        Walk32<W> w32 = w32full;
         if (active) {
             int bi = it.bi0, bj = it.bj0 + k;
             if (bj >= nbc) {
@@ -418,26 +529,33 @@ __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it
             base = d.buf_off + r0 * d.cols + c0;
             upr = bc / W;
             nu = br * upr;
-            if (bc != d.qcols) wk = UnitWalk(j, lanes, upr);
+            if (bc != d.qcols) {
+                wk = UnitWalk(j, lanes, upr);
+                w32 = Walk32<W>(j, lanes, upr, small ? int(d.cols) : 0);
+            }
             si = d.scale_off + int64_t(bi) * nbc + bj;
             ms_old = ms[si];
             vs_old = vs[si];
         }
-        const bool inreg = nu <= lanes * U;
+        const bool inreg = small && nu <= lanes * U;
         float pr[U][W], mr[U][W], vr[U][W];
         float mamax = 0.0f, vamax = 0.0f;
         {
             UnitWalk w1 = wk;
             if (inreg) {
+                const float *pb = params + base;
+                const float *gb = grads + base;
+                const uint8_t *mb = mc + base;
+                const uint8_t *vb = vc + base;
+                Walk32<W> w2 = w32;
 #pragma unroll
                 for (int i = 0; i < U; ++i) {
                     if (j + i * lanes < nu) {
-                        const int64_t e = base + int64_t(w1.row) * d.cols + w1.cu * W;
-                        load_f<W, true>(params, e, pr[i]);
-                        unit_moments<W, true>(s, grads, mc, vc, e, ms_old, vs_old, mr[i], vr[i],
+                        if (kLoadParamsEarly) load_f<W, true>(pb, w2.off, pr[i]);
+                        unit_moments<W, true>(s, gb, mb, vb, w2.off, ms_old, vs_old, mr[i], vr[i],
                                               mamax, vamax);
                     }
-                    w1.next();
+                    w2.next();
                 }
             } else {
                 for (int u = j; u < nu; u += lanes) {
@@ -449,10 +567,10 @@ __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it
                 }
             }
         }
-        for (int o = (lanes < 32 ? lanes : 32) >> 1; o > 0; o >>= 1) {
-            mamax = fmaxf(mamax, __shfl_xor_sync(0xFFFFFFFFu, mamax, o));
-            vamax = fmaxf(vamax, __shfl_xor_sync(0xFFFFFFFFu, vamax, o));
-        }
+        // both maxima are non-negative and NaN-free (fmaxf drops NaN), so their
+        // bit patterns order like their values: one integer max per warp group
+        mamax = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(mamax)));
+        vamax = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(vamax)));
         if (lanes > 32) {
             if ((tid & 31) == 0) red[par][tid >> 5] = make_float2(mamax, vamax);
             __syncthreads();
@@ -464,16 +582,19 @@ __device__ __forceinline__ void opt_item(const AdamScalars &s, const OptItem &it
             }
         }
         if (!active) continue;
-        const float ms_new = block_scale(mamax, 127.0f);
+        const float ms_new = block_scale_cr(mamax, 127.0f, s.i127);
         const float vs_new = __fmul_rn(vamax, 0x1p-8f);  // = RN(vamax / 256), underflow included
         const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
         const bool vzero = !(vs_new > 0.0f);
+        // the correctly rounded update needs every |m| and v <= 2^60 (lower
+        // bounds are checked per unit)
+        const bool fast = s.fast && mamax <= 0x1p60f && vamax <= 0x1p60f;
         if (dm.exact || dv.exact)
-            pass2<W, true>(s, params, grads, mc, vc, base, d.cols, j, lanes, wk, nu, inreg, ms_old,
-                           vs_old, pr, mr, vr, dm, dv, vzero);
+            pass2<W, true>(s, params, grads, mc, vc, base, d.cols, j, lanes, wk, w32, nu, inreg,
+                           ms_old, vs_old, pr, mr, vr, dm, dv, vzero, fast);
         else
-            pass2<W, false>(s, params, grads, mc, vc, base, d.cols, j, lanes, wk, nu, inreg,
-                            ms_old, vs_old, pr, mr, vr, dm, dv, vzero);
+            pass2<W, false>(s, params, grads, mc, vc, base, d.cols, j, lanes, wk, w32, nu, inreg,
+                            ms_old, vs_old, pr, mr, vr, dm, dv, vzero, fast);
         if (j == 0) {
             ms[si] = ms_new;
             vs[si] = vs_new;

@@ -88,6 +88,8 @@ class Case:
             if s.name == "w_sq":     # one all-zero block
                 r = g[int(o):int(o) + s.numel].reshape(s.rows, s.cols)
                 r[32:64, 32:64] = 0.0
+            if s.name == "w_rows":   # zeros among normal values (mixed units)
+                g[int(o):int(o) + s.numel:7] = 0.0
         return g
 
     def step(self, step, clip=False, skip=False):
