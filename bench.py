@@ -643,7 +643,9 @@ def run_adamw(stack, args, world, peak, barrier):
             "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),
             "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
             "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 28,
-            "launches_per_step": len(stack.dbufs)}
+            "launches_per_step": len(stack.dbufs),
+            "traffic_layer_launch": _traffic_for("adamw"),
+            "algorithmic_layer_launch": 28 * stack.w.groups[0].numel}
 
 
 def run_adamw8(stack, args, world, peak, barrier):
@@ -718,7 +720,9 @@ def run_adamw8(stack, args, world, peak, barrier):
             "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
             "frac_of_peak": round(gbs / world / peak, 4),
             "bytes_per_step": nbytes, "flat_elements_per_step": elems,
-            "launches_per_step": len(order)}
+            "launches_per_step": len(order),
+            "traffic_layer_launch": _traffic_for("adamw8"),
+            "algorithmic_layer_launch": kinds[0]["bytes"]}
 
 
 def run_gather(stack, args, world, peak, barrier):
@@ -771,7 +775,10 @@ def run_gather(stack, args, world, peak, barrier):
     return {"op": "dbuf_gather + dbuf_scatter (every tensor, fp32, m shard slices)",
             "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),
             "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 16,
-            "launches_per_step": 2 * len(stack.dbufs)}
+            "launches_per_step": 2 * len(stack.dbufs),
+            "traffic_layer_launch": {"gather": _traffic_for("gather"),
+                                     "scatter": _traffic_for("scatter")},
+            "algorithmic_layer_launch": 8 * stack.w.groups[0].numel}
 
 
 def run_e2e(stack, args, world):
