@@ -99,6 +99,22 @@ struct Piece {
 };
 static_assert(sizeof(Piece) == 32, "Piece layout");
 
+// One stage of the pipelined 8-bit optimizer: the box of blocks [bi0, bi0 +
+// Rb) x [bj0, bj0 + K) of tensor `tensor` (tensor-map slot `slot`), 4096
+// elements; Rb and K follow from the tensor's block shape.
+struct P8Item {
+    int32_t slot;
+    int32_t tensor;
+    int32_t bi0;
+    int32_t bj0;
+};
+static_assert(sizeof(P8Item) == 16, "P8Item layout");
+
+constexpr int kP8MaxTensors = 16;      // tensors with tensor maps per launch (4 maps each)
+constexpr int kP8ComputeWarps = 16;    // compute warps per CTA of the pipelined kernel
+constexpr int kP8UnitsPerThread = 4;   // units of 4 elements per compute thread and stage
+constexpr int kP8StageElems = kP8ComputeWarps * 32 * 4 * kP8UnitsPerThread;  // elements per stage
+
 // Moment units (4 elements on the vector path) that one thread of the 8-bit
 // optimizer keeps in registers; larger blocks are recomputed in a second pass.
 constexpr int kOptUnitsPerLane = 2;
@@ -118,6 +134,7 @@ struct DeviceTables {
     OptItem *opt_items = nullptr;    // 8-bit optimizer: blocks of quantised tensors
     int32_t *opt_plain = nullptr;    // 8-bit optimizer: chunks of the other tensors
     Piece *pieces = nullptr;         // gather / scatter: chunks split at shard bounds
+    P8Item *p8_items = nullptr;      // pipelined 8-bit optimizer stages
     int32_t *status = nullptr;       // device status word (0, or DBUF_ETIMEOUT)
     void *base = nullptr;
     size_t bytes = 0;
@@ -157,6 +174,7 @@ size_t norm_workspace_bytes(const dbuf_plan_t *p);
 // One-time per-device set-up of the quantisation kernels (shared memory
 // limits); called from dbuf_plan_upload.  Returns a cudaError_t value.
 int prepare_quant_kernels();
+int prepare_optim_kernels();
 
 // Keeps a cudaError_t for dbuf_last_cuda_error() (per host thread).
 void record_cuda_error(int e);
@@ -187,6 +205,9 @@ struct dbuf_plan {
     std::vector<dbuf::OptItem> opt_items;
     std::vector<int32_t> opt_plain;      // chunk ids of tensors without quantisation
     std::vector<dbuf::Piece> pieces;
+    std::vector<dbuf::P8Item> p8_items;
+    std::vector<int32_t> p8_tensors;     // slot -> tensor id
+    size_t n_opt_rest = 0;               // opt_items[0, n_opt_rest): tensors without p8 items
     std::vector<int64_t> state_offsets;  // [n], -1 for quantised tensors
     int64_t n_state = 0;
 

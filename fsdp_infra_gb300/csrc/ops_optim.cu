@@ -27,7 +27,10 @@
 // moments in pass 2 instead).  Unquantised tensors keep compact fp32 moments and
 // take the fp32 path in the same launch.  16 bytes per element (read p, g and
 // two codes; write p and two codes) plus 16 bytes per block.
+#include <algorithm>
+
 #include "quant_math.cuh"
+#include "tma.cuh"
 
 namespace dbuf {
 namespace {
@@ -633,6 +636,253 @@ __global__ void __launch_bounds__(kThreads, 4)
         opt_item<1>(s, it, d, params, grads, mc, vc, ms, vs, red);
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined 8-bit AdamW.  One CTA per SM: 16 compute warps and one producer
+// warp.  The producer fetches each stage -- a box of whole quantisation blocks
+// holding 4096 elements of one tensor -- with four 2-D tensor-map copies (p,
+// g, m codes, v codes) into one of kP8Stages shared-memory buffers, completing
+// on the buffer's "full" mbarrier.  Compute threads take 8 elements (two units
+// of 4 per unit) of one block each: they read them from shared memory, release the
+// buffer on its "empty" mbarrier (one arrival per warp), step the moments,
+// meet their block's maxima (integer max per warp group; across warps through
+// shared memory and a named barrier per block), and store the parameters and
+// codes to HBM.  Every wait is bounded; a block group decides a failed wait
+// together before its next barrier, records DBUF_ETIMEOUT and stops, and the
+// producer waits (bounded) for its own copies before the CTA exits.
+// ---------------------------------------------------------------------------
+constexpr int kP8Compute = kP8ComputeWarps;
+constexpr int kP8Threads = (kP8Compute + 1) * 32;    // + the producer warp
+constexpr int kP8U = kP8UnitsPerThread;
+constexpr int kP8StageBytes = kP8StageElems * 10;    // p, g (fp32) + m, v codes
+constexpr int kP8Stages = kP8StageBytes > 60000 ? 2 : 4;
+constexpr size_t kP8SmemBytes =
+    size_t(kP8Stages) * kP8StageBytes + 1024 + 2 * kP8Stages * 8 + 16 * kP8Compute * 8;
+
+struct P8Maps {
+    CUtensorMap map[kP8MaxTensors][4];  // p, g, m codes, v codes
+};
+
+// Stage geometry of a tensor: blocks per stage nblk = Rb x K, box width bw.
+struct P8Geom {
+    int lanes, lg_lanes, K, lg_K, bw, ucols, lg_ucols;
+};
+
+__device__ __forceinline__ P8Geom p8_geom(const TensorDesc &d) {
+    P8Geom g;
+    const int qe = d.qrows * d.qcols;
+    g.lanes = qe / (4 * kP8U);
+    g.lg_lanes = __ffs(g.lanes) - 1;
+    const int nblk = kP8StageElems / qe;
+    g.K = min(256 / d.qcols, nblk);
+    g.lg_K = __ffs(g.K) - 1;
+    g.bw = g.K * d.qcols;
+    g.ucols = d.qcols >> 2;
+    g.lg_ucols = __ffs(g.ucols) - 1;
+    return g;
+}
+
+// OR of `pred` over the `count` threads of named barrier `id` (a block group).
+__device__ __forceinline__ bool group_any(bool pred, int id, int count) {
+    int r;
+    asm volatile(
+        "{\n"
+        ".reg .pred p, q;\n"
+        "setp.ne.s32 p, %1, 0;\n"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n"
+        "selp.s32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(int(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void group_sync(int id, int count) {
+    asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+__global__ void __launch_bounds__(kP8Threads, 1)
+    adamw8_pipe_kernel(const __grid_constant__ P8Maps maps, const P8Item *__restrict__ items,
+                       int nitems, const TensorDesc *__restrict__ td, float *__restrict__ params,
+                       uint8_t *__restrict__ mc, uint8_t *__restrict__ vc, float *__restrict__ ms,
+                       float *__restrict__ vs, const dbuf_adamw_hparams hp,
+                       const float *__restrict__ total_norm, const int32_t *__restrict__ nonfinite,
+                       int32_t *__restrict__ status) {
+    extern __shared__ unsigned char smem_raw[];
+    char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + size_t(kP8Stages) * kP8StageBytes);
+    uint64_t *empty = full + kP8Stages;
+    // block maxima across warps: one row of slots per named barrier, so that a
+    // slot is only ever shared by the warps of one group (kP8Compute each)
+    float2 *red = reinterpret_cast<float2 *>(empty + kP8Stages);  // [16][kP8Compute]
+    const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+    const int G = int(gridDim.x);
+    if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
+    if (tid == 0) {
+        for (int st = 0; st < kP8Stages; ++st) {
+            mbar_init(&full[st], 1);
+            mbar_init(&empty[st], kP8Compute);
+        }
+        mbar_fence_init();
+    }
+    __syncthreads();
+
+    if (warp == kP8Compute) {
+        // ---- producer ----
+        if (lane != 0) return;
+        int k = 0;
+        bool ok = true;
+        for (int i = int(blockIdx.x); i < nitems; i += G, ++k) {
+            const int st = k % kP8Stages;
+            if (k >= kP8Stages &&
+                !mbar_wait_bounded(&empty[st], uint32_t(k / kP8Stages - 1) & 1u)) {
+                ok = false;
+                break;
+            }
+            const P8Item it = items[i];
+            const TensorDesc &d = td[it.tensor];
+            const int x = it.bj0 * d.qcols, y = it.bi0 * d.qrows;
+            char *buf = stages + size_t(st) * kP8StageBytes;
+            mbar_arrive_expect_tx(&full[st], uint32_t(kP8StageBytes));
+            tma_load_2d(buf, &maps.map[it.slot][0], x, y, &full[st]);
+            tma_load_2d(buf + kP8StageElems * 4, &maps.map[it.slot][1], x, y, &full[st]);
+            tma_load_2d(buf + kP8StageElems * 8, &maps.map[it.slot][2], x, y, &full[st]);
+            tma_load_2d(buf + kP8StageElems * 9, &maps.map[it.slot][3], x, y, &full[st]);
+        }
+        if (!ok) atomicExch(status, DBUF_ETIMEOUT);
+        // the copies of the last stage issued into each buffer may still be in
+        // flight: wait for them (bounded) before the CTA exits
+        for (int j = (k > kP8Stages ? k - kP8Stages : 0); j < k; ++j)
+            (void)mbar_wait_bounded(&full[j % kP8Stages], uint32_t(j / kP8Stages) & 1u);
+        return;
+    }
+
+    // ---- compute ----
+    const AdamScalars s = adam_scalars(hp, total_norm);
+    int k = 0;
+    for (int i = int(blockIdx.x); i < nitems; i += G, ++k) {
+        const int st = k % kP8Stages;
+        const P8Item it = items[i];
+        const TensorDesc &d = td[it.tensor];
+        const P8Geom g = p8_geom(d);
+        const int bl = tid >> g.lg_lanes, j = tid & (g.lanes - 1);
+        const int rb = bl >> g.lg_K, kb = bl & (g.K - 1);
+        const int bi = it.bi0 + rb, bj = it.bj0 + kb;
+        const bool block = int64_t(bi) * d.qrows < d.rows && bj < d.nbc;
+        const int64_t si = d.scale_off + int64_t(bi) * d.nbc + bj;
+        float ms_old = 0.0f, vs_old = 0.0f;
+        if (block) {
+            ms_old = ms[si];
+            vs_old = vs[si];
+        }
+        const bool got = mbar_wait_bounded(&full[st], uint32_t(k / kP8Stages) & 1u);
+
+        // this thread's two units: element offsets in the stage and in HBM
+        const char *buf = stages + size_t(st) * kP8StageBytes;
+        float p[kP8U][4], m[kP8U][4], v[kP8U][4];
+        int64_t e[kP8U];
+        bool valid[kP8U];
+        float mamax = 0.0f, vamax = 0.0f;
+        uint32_t cmw[kP8U], cvw[kP8U];
+        float gw[kP8U][4];
+#pragma unroll
+        for (int u2 = 0; u2 < kP8U; ++u2) {
+            const int u = j + u2 * g.lanes;
+            const int row = u >> g.lg_ucols, cq = u & (g.ucols - 1);
+            const int so = (rb * d.qrows + row) * g.bw + kb * d.qcols + 4 * cq;
+            const int64_t r = int64_t(bi) * d.qrows + row;
+            const int c = bj * d.qcols + 4 * cq;
+            valid[u2] = block && r < d.rows && c < d.cols;
+            e[u2] = d.buf_off + r * d.cols + c;
+            const float4 pp = *reinterpret_cast<const float4 *>(buf + size_t(so) * 4);
+            const float4 gg = *reinterpret_cast<const float4 *>(buf + kP8StageElems * 4 + size_t(so) * 4);
+            p[u2][0] = pp.x; p[u2][1] = pp.y; p[u2][2] = pp.z; p[u2][3] = pp.w;
+            gw[u2][0] = gg.x; gw[u2][1] = gg.y; gw[u2][2] = gg.z; gw[u2][3] = gg.w;
+            cmw[u2] = *reinterpret_cast<const uint32_t *>(buf + kP8StageElems * 8 + so);
+            cvw[u2] = *reinterpret_cast<const uint32_t *>(buf + kP8StageElems * 9 + so);
+        }
+        // the buffer may be refilled once every warp has its data in registers
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[st]);
+
+#pragma unroll
+        for (int u2 = 0; u2 < kP8U; ++u2) {
+            const uint32_t xm = cmw[u2] ^ 0x80808080u;
+            const float2 om = splat(-8388736.0f), ov = splat(-8388607.0f);
+            const float2 sm = splat(ms_old), sv = splat(vs_old);
+            const float2 m01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 0), byte_float(xm, 1)), om), sm);
+            const float2 m23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 2), byte_float(xm, 3)), om), sm);
+            const float2 v01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cvw[u2], 0), byte_float(cvw[u2], 1)), ov), sv);
+            const float2 v23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cvw[u2], 2), byte_float(cvw[u2], 3)), ov), sv);
+            m[u2][0] = m01.x; m[u2][1] = m01.y; m[u2][2] = m23.x; m[u2][3] = m23.y;
+            v[u2][0] = v01.x; v[u2][1] = v01.y; v[u2][2] = v23.x; v[u2][3] = v23.y;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) adam_moments(s, gw[u2][w], m[u2][w], v[u2][w]);
+            if (valid[u2]) {
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    mamax = fmaxf(mamax, fabsf(m[u2][w]));
+                    vamax = fmaxf(vamax, v[u2][w]);
+                }
+            }
+        }
+
+        // block maxima and the group's verdict on the wait.  Each group size has
+        // its own named barriers (64 threads: ids 1-8, 128: 9-12, 256: 13-14,
+        // 512: 15), so an id always joins the same warps with the same count.
+        bool failed;
+        const int id_base = g.lanes == 64 ? 1 : g.lanes == 128 ? 9 : g.lanes == 256 ? 13 : 15;
+        const int gid = id_base + (tid >> g.lg_lanes);
+        if (g.lanes <= 32) {
+            const unsigned gmask = g.lanes == 32
+                                       ? 0xFFFFFFFFu
+                                       : ((1u << g.lanes) - 1u) << (lane & ~(g.lanes - 1));
+            failed = __any_sync(gmask, !got);
+            mamax = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(mamax)));
+            vamax = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(vamax)));
+        } else {
+            failed = group_any(!got, gid, g.lanes);
+            mamax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mamax)));
+            vamax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(vamax)));
+            const int w0 = (bl << g.lg_lanes) >> 5;
+            if (lane == 0) red[gid * kP8Compute + (warp - w0)] = make_float2(mamax, vamax);
+            group_sync(gid, g.lanes);
+            for (int q = 0; q < (g.lanes >> 5); ++q) {
+                const float2 r = red[gid * kP8Compute + q];
+                mamax = fmaxf(mamax, r.x);
+                vamax = fmaxf(vamax, r.y);
+            }
+        }
+        if (failed) {
+            if (j == 0) atomicExch(status, DBUF_ETIMEOUT);
+            break;
+        }
+        if (!block) continue;
+
+        const float ms_new = block_scale_cr(mamax, 127.0f, s.i127);
+        const float vs_new = __fmul_rn(vamax, 0x1p-8f);
+        const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
+        const bool vzero = !(vs_new > 0.0f);
+        const bool fast = s.fast && mamax <= 0x1p60f && vamax <= 0x1p60f;
+        const bool exact = dm.exact || dv.exact;
+#pragma unroll
+        for (int u2 = 0; u2 < kP8U; ++u2) {
+            if (!valid[u2]) continue;
+            if (exact)
+                unit_update<4, true>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv, vzero,
+                                     fast);
+            else
+                unit_update<4, false>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv, vzero,
+                                      fast);
+        }
+        if (j == 0) {
+            ms[si] = ms_new;
+            vs[si] = vs_new;
+        }
+    }
+}
+
 }  // namespace
 
 int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
@@ -646,13 +896,45 @@ int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float 
     return cudaGetLastError();
 }
 
+int prepare_optim_kernels() {
+    return int(cudaFuncSetAttribute(adamw8_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    int(kP8SmemBytes)));
+}
+
 int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8_t *m_codes,
                   uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
                   const dbuf_adamw_hparams &hp, const float *total_norm, const int32_t *nonfinite,
                   void *stream) {
-    const size_t grid = p->opt_plain.size() + p->opt_items.size();
-    if (grid == 0) return cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The pipelined kernel takes the tensors with tensor maps when every buffer
+    // is 16-byte aligned and the maps encode; the register kernel takes the rest
+    // (all quantised tensors otherwise).
+    const uintptr_t bits = reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(grads) |
+                           reinterpret_cast<uintptr_t>(m_codes) | reinterpret_cast<uintptr_t>(v_codes);
+    bool pipe = !p->p8_items.empty() && (bits & 15) == 0;
+    P8Maps maps;
+    for (size_t slot = 0; pipe && slot < p->p8_tensors.size(); ++slot) {
+        const TensorDesc &d = p->tdesc[p->p8_tensors[slot]];
+        const int qe = d.qrows * d.qcols, nblk = kP8StageElems / qe;
+        const int K = std::min(256 / d.qcols, nblk), bw = K * d.qcols, bh = (nblk / K) * d.qrows;
+        pipe = encode_map_2d(&maps.map[slot][0], true, params + d.buf_off, d.cols, d.rows, bw, bh) &&
+               encode_map_2d(&maps.map[slot][1], true, const_cast<float *>(grads) + d.buf_off,
+                             d.cols, d.rows, bw, bh) &&
+               encode_map_2d(&maps.map[slot][2], false, m_codes + d.buf_off, d.cols, d.rows, bw, bh) &&
+               encode_map_2d(&maps.map[slot][3], false, v_codes + d.buf_off, d.cols, d.rows, bw, bh);
+    }
+    const size_t n_items = pipe ? p->n_opt_rest : p->opt_items.size();
+    const size_t grid = p->opt_plain.size() + n_items;
+    if (pipe) {
+        const int n = int(p->p8_items.size());
+        const int g = n < p->dev.num_sms ? n : p->dev.num_sms;
+        adamw8_pipe_kernel<<<g, kP8Threads, kP8SmemBytes, st>>>(
+            maps, p->dev.p8_items, n, p->dev.tensors, params, m_codes, v_codes, m_scales, v_scales,
+            hp, total_norm, nonfinite, p->dev.status);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    if (grid == 0) return cudaSuccess;
     adamw8_kernel<<<unsigned(grid), kThreads, 0, st>>>(
         p->dev.chunks, p->dev.opt_plain, int32_t(p->opt_plain.size()), p->dev.opt_items,
         p->dev.tensors, params, grads, m_codes, v_codes, m_scales, v_scales, m32, v32, hp,

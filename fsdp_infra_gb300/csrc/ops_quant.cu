@@ -30,6 +30,7 @@
 #include <mutex>
 
 #include "quant_math.cuh"
+#include "tma.cuh"
 
 namespace dbuf {
 namespace {
@@ -300,62 +301,10 @@ constexpr int kPipeStages = 3;
 constexpr int kPipeStageBytes = kPipeMaxRows * kPipeMaxCols * 4;
 constexpr int kPipeRowsPerWarp = kPipeMaxRows / kPipeWarps;
 constexpr size_t kPipeSmemBytes = size_t(kPipeStages) * kPipeStageBytes + 1024 + 256;
-constexpr uint32_t kWaitLimit = 1u << 22;
 
 struct TmaMaps {
     CUtensorMap map[kPipeMaxTensors];
 };
-
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_fence_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n"
-        ".reg .pred p;\n"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n"
-        "}\n"
-        : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return done != 0;
-}
-
-// Waits for the phase of `parity` to complete, giving up after kWaitLimit tries.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
-        if (mbar_try_wait(bar, parity)) return true;
-    return false;
-}
-
-// The box of tensor map `map` at element coordinates (x = column, y = row)
-// into this CTA's shared memory, completing on `bar`.
-__device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *map, int x, int y,
-                                            uint64_t *bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_u32(smem_dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
-        : "memory");
-}
 
 struct PipeTile {
     uint8_t *y;
@@ -504,6 +453,21 @@ PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
 }  // namespace
 
+bool encode_map_2d(CUtensorMap *map, bool f32, void *base, int64_t cols, int64_t rows,
+                   int box_cols, int box_rows) {
+    if (!g_encode) return false;
+    const int es = f32 ? 4 : 1;
+    const cuuint64_t dims[2] = {cuuint64_t(cols), cuuint64_t(rows)};
+    const cuuint64_t strides[1] = {cuuint64_t(cols) * cuuint64_t(es)};
+    const cuuint32_t box[2] = {cuuint32_t(box_cols), cuuint32_t(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(map, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                                2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                                CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
 int prepare_quant_kernels() {
     cudaError_t e = cudaFuncSetAttribute(quant_pipe_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -527,19 +491,11 @@ namespace {
 // Tensor maps of the pipelined tensors of `p` over the buffer `buf` (one 2-D
 // map per tensor: columns x rows, row pitch cols*4 bytes, box qcols x qrows).
 bool encode_maps(const dbuf_plan_t *p, const float *buf, TmaMaps *maps) {
-    if (!g_encode) return false;
     for (size_t slot = 0; slot < p->pipe_tensors.size(); ++slot) {
         const TensorDesc &d = p->tdesc[p->pipe_tensors[slot]];
-        const cuuint64_t dims[2] = {cuuint64_t(d.cols), cuuint64_t(d.rows)};
-        const cuuint64_t strides[1] = {cuuint64_t(d.cols) * 4u};
-        const cuuint32_t box[2] = {cuuint32_t(d.qcols), cuuint32_t(d.qrows)};
-        const cuuint32_t estr[2] = {1, 1};
-        void *base = const_cast<float *>(buf + d.buf_off);
-        const CUresult r = g_encode(&maps->map[slot], CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims,
-                                    strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                                    CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return false;
+        if (!encode_map_2d(&maps->map[slot], true, const_cast<float *>(buf + d.buf_off), d.cols,
+                           d.rows, d.qcols, d.qrows))
+            return false;
     }
     return true;
 }

@@ -230,6 +230,9 @@ void build_tables(dbuf_plan_t *p) {
     p->pipe_tensors.clear();
     p->opt_items.clear();
     p->opt_plain.clear();
+    p->p8_items.clear();
+    p->p8_tensors.clear();
+    std::vector<dbuf::OptItem> p8_opt;  // register-kernel items of p8 tensors (the fallback)
     p->state_offsets.assign(n, -1);
     int64_t s_off = 0, st_off = 0;
     for (int32_t t = 0; t < n; ++t) {
@@ -274,10 +277,31 @@ void build_tables(dbuf_plan_t *p) {
                 int64_t per = std::max<int64_t>(1, dbuf::kOptItemElems / std::max<int64_t>(1, be));
                 per = std::max<int64_t>(groups, (per + groups - 1) / groups * groups);
                 per = std::min<int64_t>(per, 16384);
+                // The pipelined kernel takes power-of-two blocks of at most one stage
+                // (and at least one unit of every compute thread of a block group)
+                // whose rows are 16-byte aligned in every buffer (fp32 and codes).
+                auto pow2 = [](int64_t x) { return x > 0 && (x & (x - 1)) == 0; };
+                const bool p8 = pow2(d.qrows) && pow2(d.qcols) && d.qcols >= 16 && d.qcols <= 256 &&
+                                be <= dbuf::kP8StageElems && be >= 4 * dbuf::kP8UnitsPerThread &&
+                                s.cols % 16 == 0 &&
+                                d.buf_off % 16 == 0 && s.rows < (int64_t(1) << 31) &&
+                                s.cols < (int64_t(1) << 31) &&
+                                p->p8_tensors.size() < size_t(dbuf::kP8MaxTensors);
+                std::vector<dbuf::OptItem> &dst = p8 ? p8_opt : p->opt_items;
                 for (int64_t b = 0; b < nb; b += per)
-                    p->opt_items.push_back(dbuf::OptItem{t, int32_t(b / d.nbc), int32_t(b % d.nbc),
-                                                         int16_t(std::min(per, nb - b)),
-                                                         int16_t(lanes)});
+                    dst.push_back(dbuf::OptItem{t, int32_t(b / d.nbc), int32_t(b % d.nbc),
+                                                int16_t(std::min(per, nb - b)), int16_t(lanes)});
+                if (p8) {
+                    const int32_t slot = int32_t(p->p8_tensors.size());
+                    p->p8_tensors.push_back(t);
+                    const int64_t nblk = dbuf::kP8StageElems / be;
+                    const int64_t K = std::min<int64_t>(256 / d.qcols, nblk);
+                    const int64_t Rb = nblk / K;
+                    for (int64_t bi = 0; bi < nbr; bi += Rb)
+                        for (int64_t bj = 0; bj < d.nbc; bj += K)
+                            p->p8_items.push_back(
+                                dbuf::P8Item{slot, t, int32_t(bi), int32_t(bj)});
+                }
             }
             if (d.qrows == 1) {
                 for (int64_t b = 0; b < nb; b += dbuf::kRowItemBlocks)
@@ -308,6 +332,8 @@ void build_tables(dbuf_plan_t *p) {
     }
     p->n_scales = s_off;
     p->n_state = st_off;
+    p->n_opt_rest = p->opt_items.size();
+    p->opt_items.insert(p->opt_items.end(), p8_opt.begin(), p8_opt.end());
 
     // gather / scatter pieces: each tensor's chunks cut again at shard bounds
     p->pieces.clear();
@@ -403,7 +429,7 @@ extern "C" int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
         if (p->chunks.size() > size_t(INT32_MAX) || p->tile_items.size() > size_t(INT32_MAX) ||
             p->row_items.size() > size_t(INT32_MAX) || p->pipe_items.size() > size_t(INT32_MAX) ||
             p->opt_items.size() + p->opt_plain.size() > size_t(INT32_MAX) ||
-            p->pieces.size() > size_t(INT32_MAX)) {
+            p->pieces.size() > size_t(INT32_MAX) || p->p8_items.size() > size_t(INT32_MAX)) {
             delete p;
             return DBUF_ERANGE;
         }
