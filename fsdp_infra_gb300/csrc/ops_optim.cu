@@ -637,49 +637,44 @@ __global__ void __launch_bounds__(kThreads, 4)
 }
 
 // ---------------------------------------------------------------------------
-// Pipelined 8-bit AdamW.  One CTA per SM: 16 compute warps and one producer
-// warp.  The producer fetches each stage -- a box of whole quantisation blocks
-// holding 4096 elements of one tensor -- with four 2-D tensor-map copies (p,
-// g, m codes, v codes) into one of kP8Stages shared-memory buffers, completing
-// on the buffer's "full" mbarrier.  Compute threads take 8 elements (two units
-// of 4 per unit) of one block each: they read them from shared memory, release the
-// buffer on its "empty" mbarrier (one arrival per warp), step the moments,
-// meet their block's maxima (integer max per warp group; across warps through
-// shared memory and a named barrier per block), and store the parameters and
-// codes to HBM.  Every wait is bounded; a block group decides a failed wait
-// together before its next barrier, records DBUF_ETIMEOUT and stops, and the
-// producer waits (bounded) for its own copies before the CTA exits.
+// Pipelined 8-bit AdamW.  One CTA of 16 warps per SM.  Each stage is a box of
+// whole quantisation blocks of one tensor holding kP8StageElems elements,
+// fetched with four 2-D tensor-map copies (p, g, m codes, v codes) into one of
+// two shared-memory buffers and completing on the buffer's "full" mbarrier.
+// Thread 0 issues the copies of stage k+2 into the buffer of stage k as soon
+// as every warp has released it (its "empty" mbarrier, one arrival per warp,
+// after the warp has its data in registers).  Every thread takes 16
+// elements (four units of 4) of one block: it steps the moments, the block's
+// threads meet their maxima (integer max within a warp; across warps through
+// shared memory and a named barrier whose id range belongs to one group size),
+// and it stores the parameters and codes to HBM.  Per-tensor geometry sits in
+// a shared-memory table; the next stage's item and old scales are loaded one
+// iteration ahead.  Every wait is bounded: a block group decides a failed wait
+// together before its next barrier, records DBUF_ETIMEOUT and stops; thread 0
+// stops issuing on a failed wait but keeps taking part in its group, and
+// waits (bounded) for copies still in flight before the CTA exits.
 // ---------------------------------------------------------------------------
-constexpr int kP8Compute = kP8ComputeWarps;
-constexpr int kP8Threads = (kP8Compute + 1) * 32;    // + the producer warp
+constexpr int kP8Warps = kP8ComputeWarps;
+constexpr int kP8Threads = kP8Warps * 32;
 constexpr int kP8U = kP8UnitsPerThread;
 constexpr int kP8StageBytes = kP8StageElems * 10;    // p, g (fp32) + m, v codes
-constexpr int kP8Stages = kP8StageBytes > 60000 ? 2 : 4;
-constexpr size_t kP8SmemBytes =
-    size_t(kP8Stages) * kP8StageBytes + 1024 + 2 * kP8Stages * 8 + 16 * kP8Compute * 8;
+constexpr int kP8Stages = 2;
 
 struct P8Maps {
     CUtensorMap map[kP8MaxTensors][4];  // p, g, m codes, v codes
+    int32_t tensor[kP8MaxTensors];      // slot -> tensor
+    int32_t nslots;
 };
 
-// Stage geometry of a tensor: blocks per stage nblk = Rb x K, box width bw.
-struct P8Geom {
-    int lanes, lg_lanes, K, lg_K, bw, ucols, lg_ucols;
+// Geometry of one tensor's stages: blocks per stage nblk = Rb x K, box width bw.
+struct P8Slot {
+    int64_t buf_off, rows, cols, scale_off;
+    int qrows, qcols, nbc, lanes, lg_lanes, K, lg_K, bw, ucols, lg_ucols, id_base, pad;
 };
 
-__device__ __forceinline__ P8Geom p8_geom(const TensorDesc &d) {
-    P8Geom g;
-    const int qe = d.qrows * d.qcols;
-    g.lanes = qe / (4 * kP8U);
-    g.lg_lanes = __ffs(g.lanes) - 1;
-    const int nblk = kP8StageElems / qe;
-    g.K = min(256 / d.qcols, nblk);
-    g.lg_K = __ffs(g.K) - 1;
-    g.bw = g.K * d.qcols;
-    g.ucols = d.qcols >> 2;
-    g.lg_ucols = __ffs(g.ucols) - 1;
-    return g;
-}
+constexpr size_t kP8SmemBytes = size_t(kP8Stages) * kP8StageBytes + 1024 +
+                                2 * kP8Stages * 8 + 16 * kP8Warps * 8 +
+                                kP8MaxTensors * sizeof(P8Slot);
 
 // OR of `pred` over the `count` threads of named barrier `id` (a block group).
 __device__ __forceinline__ bool group_any(bool pred, int id, int count) {
@@ -701,6 +696,37 @@ __device__ __forceinline__ void group_sync(int id, int count) {
     asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// The block of stage item `it` that thread `tid` works on, and its scale index.
+struct P8Place {
+    int bl, j, rb, kb, bi, bj;
+    bool block;
+    int64_t si;
+};
+
+__device__ __forceinline__ P8Place p8_place(const P8Slot &g, const P8Item &it, int tid) {
+    P8Place q;
+    q.bl = tid >> g.lg_lanes;
+    q.j = tid & (g.lanes - 1);
+    q.rb = q.bl >> g.lg_K;
+    q.kb = q.bl & (g.K - 1);
+    q.bi = it.bi0 + q.rb;
+    q.bj = it.bj0 + q.kb;
+    q.block = int64_t(q.bi) * g.qrows < g.rows && q.bj < g.nbc;
+    q.si = g.scale_off + int64_t(q.bi) * g.nbc + q.bj;
+    return q;
+}
+
+__device__ __forceinline__ void p8_issue(const P8Maps &maps, const P8Slot *slots, const P8Item &it,
+                                         char *buf, uint64_t *full) {
+    const P8Slot &g = slots[it.slot];
+    const int x = it.bj0 * g.qcols, y = it.bi0 * g.qrows;
+    mbar_arrive_expect_tx(full, uint32_t(kP8StageBytes));
+    tma_load_2d(buf, &maps.map[it.slot][0], x, y, full);
+    tma_load_2d(buf + kP8StageElems * 4, &maps.map[it.slot][1], x, y, full);
+    tma_load_2d(buf + kP8StageElems * 8, &maps.map[it.slot][2], x, y, full);
+    tma_load_2d(buf + kP8StageElems * 9, &maps.map[it.slot][3], x, y, full);
+}
+
 __global__ void __launch_bounds__(kP8Threads, 1)
     adamw8_pipe_kernel(const __grid_constant__ P8Maps maps, const P8Item *__restrict__ items,
                        int nitems, const TensorDesc *__restrict__ td, float *__restrict__ params,
@@ -714,71 +740,80 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     uint64_t *full = reinterpret_cast<uint64_t *>(stages + size_t(kP8Stages) * kP8StageBytes);
     uint64_t *empty = full + kP8Stages;
     // block maxima across warps: one row of slots per named barrier, so that a
-    // slot is only ever shared by the warps of one group (kP8Compute each)
-    float2 *red = reinterpret_cast<float2 *>(empty + kP8Stages);  // [16][kP8Compute]
+    // slot is only ever shared by the warps of one group
+    float2 *red = reinterpret_cast<float2 *>(empty + kP8Stages);  // [16][kP8Warps]
+    P8Slot *slots = reinterpret_cast<P8Slot *>(red + 16 * kP8Warps);
     const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
     const int G = int(gridDim.x);
     if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
+    if (tid < maps.nslots) {
+        const TensorDesc &d = td[maps.tensor[tid]];
+        P8Slot g;
+        g.buf_off = d.buf_off;
+        g.rows = d.rows;
+        g.cols = d.cols;
+        g.scale_off = d.scale_off;
+        g.qrows = d.qrows;
+        g.qcols = d.qcols;
+        g.nbc = d.nbc;
+        const int qe = d.qrows * d.qcols;
+        g.lanes = qe / (4 * kP8U);
+        g.lg_lanes = __ffs(g.lanes) - 1;
+        const int nblk = kP8StageElems / qe;
+        g.K = min(256 / d.qcols, nblk);
+        g.lg_K = __ffs(g.K) - 1;
+        g.bw = g.K * d.qcols;
+        g.ucols = d.qcols >> 2;
+        g.lg_ucols = __ffs(g.ucols) - 1;
+        g.id_base = g.lanes == 64 ? 1 : g.lanes == 128 ? 9 : g.lanes == 256 ? 13 : 15;
+        g.pad = 0;
+        slots[tid] = g;
+    }
     if (tid == 0) {
         for (int st = 0; st < kP8Stages; ++st) {
             mbar_init(&full[st], 1);
-            mbar_init(&empty[st], kP8Compute);
+            mbar_init(&empty[st], kP8Warps);
         }
         mbar_fence_init();
     }
     __syncthreads();
-
-    if (warp == kP8Compute) {
-        // ---- producer ----
-        if (lane != 0) return;
-        int k = 0;
-        bool ok = true;
-        for (int i = int(blockIdx.x); i < nitems; i += G, ++k) {
-            const int st = k % kP8Stages;
-            if (k >= kP8Stages &&
-                !mbar_wait_bounded(&empty[st], uint32_t(k / kP8Stages - 1) & 1u)) {
-                ok = false;
-                break;
-            }
-            const P8Item it = items[i];
-            const TensorDesc &d = td[it.tensor];
-            const int x = it.bj0 * d.qcols, y = it.bi0 * d.qrows;
-            char *buf = stages + size_t(st) * kP8StageBytes;
-            mbar_arrive_expect_tx(&full[st], uint32_t(kP8StageBytes));
-            tma_load_2d(buf, &maps.map[it.slot][0], x, y, &full[st]);
-            tma_load_2d(buf + kP8StageElems * 4, &maps.map[it.slot][1], x, y, &full[st]);
-            tma_load_2d(buf + kP8StageElems * 8, &maps.map[it.slot][2], x, y, &full[st]);
-            tma_load_2d(buf + kP8StageElems * 9, &maps.map[it.slot][3], x, y, &full[st]);
-        }
-        if (!ok) atomicExch(status, DBUF_ETIMEOUT);
-        // the copies of the last stage issued into each buffer may still be in
-        // flight: wait for them (bounded) before the CTA exits
-        for (int j = (k > kP8Stages ? k - kP8Stages : 0); j < k; ++j)
-            (void)mbar_wait_bounded(&full[j % kP8Stages], uint32_t(j / kP8Stages) & 1u);
-        return;
-    }
-
-    // ---- compute ----
     const AdamScalars s = adam_scalars(hp, total_norm);
-    int k = 0;
-    for (int i = int(blockIdx.x); i < nitems; i += G, ++k) {
-        const int st = k % kP8Stages;
-        const P8Item it = items[i];
-        const TensorDesc &d = td[it.tensor];
-        const P8Geom g = p8_geom(d);
-        const int bl = tid >> g.lg_lanes, j = tid & (g.lanes - 1);
-        const int rb = bl >> g.lg_K, kb = bl & (g.K - 1);
-        const int bi = it.bi0 + rb, bj = it.bj0 + kb;
-        const bool block = int64_t(bi) * d.qrows < d.rows && bj < d.nbc;
-        const int64_t si = d.scale_off + int64_t(bi) * d.nbc + bj;
-        float ms_old = 0.0f, vs_old = 0.0f;
-        if (block) {
-            ms_old = ms[si];
-            vs_old = vs[si];
+    const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
+    if (mine == 0) return;
+    bool issuing = true;  // thread 0: still issuing copies
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < kP8Stages && issued < mine; ++issued)
+            p8_issue(maps, slots, items[int(blockIdx.x) + issued * G],
+                     stages + size_t(issued) * kP8StageBytes, &full[issued]);
+
+    P8Item cur = items[blockIdx.x];
+    float ms_cur = 0.0f, vs_cur = 0.0f;
+    {
+        const P8Place q = p8_place(slots[cur.slot], cur, tid);
+        if (q.block) {
+            ms_cur = ms[q.si];
+            vs_cur = vs[q.si];
         }
+    }
+    for (int k = 0; k < mine; ++k) {
+        const int st = k % kP8Stages;
+        // the next item and its old scales, one iteration ahead
+        P8Item nxt = cur;
+        float ms_nxt = 0.0f, vs_nxt = 0.0f;
+        if (k + 1 < mine) {
+            nxt = items[int(blockIdx.x) + (k + 1) * G];
+            const P8Place qn = p8_place(slots[nxt.slot], nxt, tid);
+            if (qn.block) {
+                ms_nxt = ms[qn.si];
+                vs_nxt = vs[qn.si];
+            }
+        }
+
+        const P8Slot &g = slots[cur.slot];
+        const P8Place q = p8_place(g, cur, tid);
         const bool got = mbar_wait_bounded(&full[st], uint32_t(k / kP8Stages) & 1u);
 
-        // this thread's two units: element offsets in the stage and in HBM
         const char *buf = stages + size_t(st) * kP8StageBytes;
         float p[kP8U][4], m[kP8U][4], v[kP8U][4];
         int64_t e[kP8U];
@@ -788,29 +823,41 @@ __global__ void __launch_bounds__(kP8Threads, 1)
         float gw[kP8U][4];
 #pragma unroll
         for (int u2 = 0; u2 < kP8U; ++u2) {
-            const int u = j + u2 * g.lanes;
+            const int u = q.j + u2 * g.lanes;
             const int row = u >> g.lg_ucols, cq = u & (g.ucols - 1);
-            const int so = (rb * d.qrows + row) * g.bw + kb * d.qcols + 4 * cq;
-            const int64_t r = int64_t(bi) * d.qrows + row;
-            const int c = bj * d.qcols + 4 * cq;
-            valid[u2] = block && r < d.rows && c < d.cols;
-            e[u2] = d.buf_off + r * d.cols + c;
+            const int so = (q.rb * g.qrows + row) * g.bw + q.kb * g.qcols + 4 * cq;
+            const int64_t r = int64_t(q.bi) * g.qrows + row;
+            const int c = q.bj * g.qcols + 4 * cq;
+            valid[u2] = q.block && r < g.rows && c < g.cols;
+            e[u2] = g.buf_off + r * g.cols + c;
             const float4 pp = *reinterpret_cast<const float4 *>(buf + size_t(so) * 4);
-            const float4 gg = *reinterpret_cast<const float4 *>(buf + kP8StageElems * 4 + size_t(so) * 4);
+            const float4 gg =
+                *reinterpret_cast<const float4 *>(buf + kP8StageElems * 4 + size_t(so) * 4);
             p[u2][0] = pp.x; p[u2][1] = pp.y; p[u2][2] = pp.z; p[u2][3] = pp.w;
             gw[u2][0] = gg.x; gw[u2][1] = gg.y; gw[u2][2] = gg.z; gw[u2][3] = gg.w;
             cmw[u2] = *reinterpret_cast<const uint32_t *>(buf + kP8StageElems * 8 + so);
             cvw[u2] = *reinterpret_cast<const uint32_t *>(buf + kP8StageElems * 9 + so);
         }
-        // the buffer may be refilled once every warp has its data in registers
+        // the buffer may be refilled once every warp has its data in registers:
+        // thread 0 waits for all releases and issues stage k + kP8Stages into it
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty[st]);
+        if (tid == 0 && issuing && k + kP8Stages < mine) {
+            if (!mbar_wait_bounded(&empty[st], uint32_t(k / kP8Stages) & 1u)) {
+                issuing = false;
+                atomicExch(status, DBUF_ETIMEOUT);
+            } else {
+                p8_issue(maps, slots, items[int(blockIdx.x) + (k + kP8Stages) * G],
+                         stages + size_t(st) * kP8StageBytes, &full[st]);
+                ++issued;
+            }
+        }
 
 #pragma unroll
         for (int u2 = 0; u2 < kP8U; ++u2) {
             const uint32_t xm = cmw[u2] ^ 0x80808080u;
             const float2 om = splat(-8388736.0f), ov = splat(-8388607.0f);
-            const float2 sm = splat(ms_old), sv = splat(vs_old);
+            const float2 sm = splat(ms_cur), sv = splat(vs_cur);
             const float2 m01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 0), byte_float(xm, 1)), om), sm);
             const float2 m23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 2), byte_float(xm, 3)), om), sm);
             const float2 v01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cvw[u2], 0), byte_float(cvw[u2], 1)), ov), sv);
@@ -828,12 +875,8 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             }
         }
 
-        // block maxima and the group's verdict on the wait.  Each group size has
-        // its own named barriers (64 threads: ids 1-8, 128: 9-12, 256: 13-14,
-        // 512: 15), so an id always joins the same warps with the same count.
+        // block maxima and the group's verdict on the wait
         bool failed;
-        const int id_base = g.lanes == 64 ? 1 : g.lanes == 128 ? 9 : g.lanes == 256 ? 13 : 15;
-        const int gid = id_base + (tid >> g.lg_lanes);
         if (g.lanes <= 32) {
             const unsigned gmask = g.lanes == 32
                                        ? 0xFFFFFFFFu
@@ -842,44 +885,54 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             mamax = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(mamax)));
             vamax = __uint_as_float(__reduce_max_sync(gmask, __float_as_uint(vamax)));
         } else {
+            const int gid = g.id_base + q.bl;
             failed = group_any(!got, gid, g.lanes);
             mamax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mamax)));
             vamax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(vamax)));
-            const int w0 = (bl << g.lg_lanes) >> 5;
-            if (lane == 0) red[gid * kP8Compute + (warp - w0)] = make_float2(mamax, vamax);
+            const int w0 = (q.bl << g.lg_lanes) >> 5;
+            if (lane == 0) red[gid * kP8Warps + (warp - w0)] = make_float2(mamax, vamax);
             group_sync(gid, g.lanes);
-            for (int q = 0; q < (g.lanes >> 5); ++q) {
-                const float2 r = red[gid * kP8Compute + q];
+            for (int w = 0; w < (g.lanes >> 5); ++w) {
+                const float2 r = red[gid * kP8Warps + w];
                 mamax = fmaxf(mamax, r.x);
                 vamax = fmaxf(vamax, r.y);
             }
         }
         if (failed) {
-            if (j == 0) atomicExch(status, DBUF_ETIMEOUT);
+            if (q.j == 0) atomicExch(status, DBUF_ETIMEOUT);
             break;
         }
-        if (!block) continue;
-
-        const float ms_new = block_scale_cr(mamax, 127.0f, s.i127);
-        const float vs_new = __fmul_rn(vamax, 0x1p-8f);
-        const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
-        const bool vzero = !(vs_new > 0.0f);
-        const bool fast = s.fast && mamax <= 0x1p60f && vamax <= 0x1p60f;
-        const bool exact = dm.exact || dv.exact;
+        if (q.block) {
+            const float ms_new = block_scale_cr(mamax, 127.0f, s.i127);
+            const float vs_new = __fmul_rn(vamax, 0x1p-8f);
+            const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
+            const bool vzero = !(vs_new > 0.0f);
+            const bool fast = s.fast && mamax <= 0x1p60f && vamax <= 0x1p60f;
+            const bool exact = dm.exact || dv.exact;
 #pragma unroll
-        for (int u2 = 0; u2 < kP8U; ++u2) {
-            if (!valid[u2]) continue;
-            if (exact)
-                unit_update<4, true>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv, vzero,
-                                     fast);
-            else
-                unit_update<4, false>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv, vzero,
-                                      fast);
+            for (int u2 = 0; u2 < kP8U; ++u2) {
+                if (!valid[u2]) continue;
+                if (exact)
+                    unit_update<4, true>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv,
+                                         vzero, fast);
+                else
+                    unit_update<4, false>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv,
+                                          vzero, fast);
+            }
+            if (q.j == 0) {
+                ms[q.si] = ms_new;
+                vs[q.si] = vs_new;
+            }
         }
-        if (j == 0) {
-            ms[si] = ms_new;
-            vs[si] = vs_new;
-        }
+        cur = nxt;
+        ms_cur = ms_nxt;
+        vs_cur = vs_nxt;
+    }
+    if (tid == 0) {
+        // copies of the last stages issued may still be in flight: wait for them
+        // (bounded) before the CTA exits
+        for (int j = (issued > kP8Stages ? issued - kP8Stages : 0); j < issued; ++j)
+            (void)mbar_wait_bounded(&full[j % kP8Stages], uint32_t(j / kP8Stages) & 1u);
     }
 }
 
@@ -913,7 +966,9 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
                            reinterpret_cast<uintptr_t>(m_codes) | reinterpret_cast<uintptr_t>(v_codes);
     bool pipe = !p->p8_items.empty() && (bits & 15) == 0;
     P8Maps maps;
+    maps.nslots = int32_t(p->p8_tensors.size());
     for (size_t slot = 0; pipe && slot < p->p8_tensors.size(); ++slot) {
+        maps.tensor[slot] = p->p8_tensors[slot];
         const TensorDesc &d = p->tdesc[p->p8_tensors[slot]];
         const int qe = d.qrows * d.qcols, nblk = kP8StageElems / qe;
         const int K = std::min(256 / d.qcols, nblk), bw = K * d.qcols, bh = (nblk / K) * d.qrows;
