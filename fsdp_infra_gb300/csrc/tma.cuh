@@ -52,11 +52,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return done != 0;
 }
 
-// Waits for the phase of `parity` to complete, giving up after kWaitLimit tries.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+// Waits for the phase of `parity` to complete, giving up after `limit` tries.
+__device__ __forceinline__ bool mbar_wait_limit(uint64_t *bar, uint32_t parity, uint32_t limit) {
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return true;
     return false;
+}
+
+// The same with the library's limit, kWaitLimit tries.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity) {
+    return mbar_wait_limit(bar, parity, kWaitLimit);
 }
 
 // The box of tensor map `map` at element coordinates (x = column, y = row)

@@ -45,8 +45,8 @@ EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_pack_cast", "dbuf_unpack", "dbuf_scale_accum_zero", "dbuf_workspace_bytes",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
            "dbuf_device_status", "dbuf_adamw_step", "dbuf_plan_state_offsets",
-           "dbuf_adamw8_step", "dbuf_order", "dbuf_gather", "dbuf_scatter", "dbuf_strerror",
-           "dbuf_last_cuda_error")
+           "dbuf_adamw8_step", "dbuf_order", "dbuf_gather", "dbuf_scatter",
+           "dbuf_selftest_wait_timeout", "dbuf_strerror", "dbuf_last_cuda_error")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -120,6 +120,8 @@ def _lib_handle():
         L.dbuf_adamw8_step.restype = ctypes.c_int
         L.dbuf_order.argtypes = [P, i32, i32, P]
         L.dbuf_order.restype = ctypes.c_int
+        L.dbuf_selftest_wait_timeout.argtypes = [P, ctypes.c_uint32, P]
+        L.dbuf_selftest_wait_timeout.restype = ctypes.c_int
         for fn in ("dbuf_gather", "dbuf_scatter"):
             getattr(L, fn).argtypes = [P, P, i32, P, P]
             getattr(L, fn).restype = ctypes.c_int
@@ -288,6 +290,12 @@ def dbuf_gather(plan: int, shard_ptrs: int, dtype: int, dst_ptrs: int, stream: i
 
 def dbuf_scatter(plan: int, src_ptrs: int, dtype: int, shard_ptrs: int, stream: int = 0) -> None:
     _check(_lib_handle().dbuf_scatter(plan, src_ptrs, dtype, shard_ptrs, stream), "dbuf_scatter")
+
+
+def dbuf_selftest_wait_timeout(plan: int, tries: int, stream: int = 0) -> None:
+    """Diagnostic: a device wait that runs out and records DBUF_ETIMEOUT."""
+    _check(_lib_handle().dbuf_selftest_wait_timeout(plan, tries, stream),
+           "dbuf_selftest_wait_timeout")
 
 
 def dbuf_device_status(plan: int, stream: int = 0) -> int:

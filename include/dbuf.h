@@ -426,6 +426,18 @@ int dbuf_gather(const dbuf_plan_t *plan, void *const *shards, int32_t dtype, voi
 int dbuf_scatter(const dbuf_plan_t *plan, const void *const *src, int32_t dtype,
                  void *const *shards, void *stream);
 
+/*
+ * dbuf_selftest_wait_timeout -- diagnostic of the bounded device-side waits
+ * (the pages have no counterpart).  Launches one CTA that waits on an
+ * mbarrier phase nothing completes, gives up after `tries` polls (1 ..
+ * 2^22), and records DBUF_ETIMEOUT in the plan's status word, as the
+ * pipelined kernels do when a tensor copy never lands; read it back with
+ * dbuf_device_status.  No fault, trap or hang is involved, and the context
+ * stays usable.  Errors: DBUF_EINVAL (plan NULL, tries out of range),
+ * DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_selftest_wait_timeout(const dbuf_plan_t *plan, uint32_t tries, void *stream);
+
 /* dbuf_strerror -- static description of a return code. */
 const char *dbuf_strerror(int code);
 

@@ -69,7 +69,10 @@ def test_operators_refuse_unuploaded_plan_without_gpu(dbuf_lib):
                      lambda: d.dbuf_block_quant(p, 0, 0, 0),
                      lambda: d.dbuf_adamw8_step(p, 0, 0, 0, 0, 0, 0, 0, 0, lr=1e-3, beta1=0.9,
                                                 beta2=0.95, eps=1e-8, weight_decay=0.0,
-                                                bias_correction1=0.1, bias_correction2=0.05)]:
+                                                bias_correction1=0.1, bias_correction2=0.05),
+                     lambda: d.dbuf_gather(p, 0, d.DBUF_F32, 0),
+                     lambda: d.dbuf_scatter(p, 0, d.DBUF_F32, 0),
+                     lambda: d.dbuf_selftest_wait_timeout(p, 100)]:
             with pytest.raises(d.DbufError) as e:
                 call()
             assert e.value.code == d.DBUF_ENOTUPLOADED
