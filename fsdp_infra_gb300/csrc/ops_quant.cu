@@ -53,10 +53,11 @@ __device__ __forceinline__ float abs_max4(float m, float4 v) {
     return max3f(max3f(m, fabsf(v.x), fabsf(v.y)), fabsf(v.z), fabsf(v.w));
 }
 
+// Maximum over the warp of non-negative, NaN-free values (block maxima of |x|
+// taken with NaN-ignoring max): their bit patterns order like the values, so
+// one integer max reduction does it.
 __device__ __forceinline__ float warp_max(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
-    return v;
+    return __uint_as_float(__reduce_max_sync(0xffffffffu, __float_as_uint(v)));
 }
 
 __device__ __forceinline__ float4 ld4(const float *p) {
@@ -374,6 +375,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     float *sh_max = reinterpret_cast<float *>(bars + kPipeStages);  // [2][kPipeWarps]
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int G = gridDim.x;
+    const float iq448 = __frcp_rn(448.0f), iq127 = __frcp_rn(127.0f);  // RN(1 / qmax)
 
     if (tid == 0) {
         for (int s = 0; s < kPipeStages; ++s) mbar_init(&bars[s], 1);
@@ -424,16 +426,13 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
                                      stages + s * kPipeStageBytes, &bars[s]);
             ++issued;
         }
-        amax = sh_max[(k & 1) * kPipeWarps + (lane % kPipeWarps)];
-#pragma unroll
-        for (int o = kPipeWarps / 2; o > 0; o >>= 1)
-            amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+        amax = warp_max(sh_max[(k & 1) * kPipeWarps + (lane % kPipeWarps)]);
         if (g.quant == DBUF_QUANT_E4M3) {
-            const float scale = block_scale(amax, QParams<DBUF_QUANT_E4M3>::qmax);
+            const float scale = block_scale_cr(amax, QParams<DBUF_QUANT_E4M3>::qmax, iq448);
             pipe_encode_store<DBUF_QUANT_E4M3>(g, v, make_divisor(scale), warp, lane);
             if (tid == 0) scales[g.scale_idx] = scale;
         } else {
-            const float scale = block_scale(amax, QParams<DBUF_QUANT_INT8>::qmax);
+            const float scale = block_scale_cr(amax, QParams<DBUF_QUANT_INT8>::qmax, iq127);
             pipe_encode_store<DBUF_QUANT_INT8>(g, v, make_divisor(scale), warp, lane);
             if (tid == 0) scales[g.scale_idx] = scale;
         }
