@@ -207,3 +207,24 @@ def test_adamw8_dense7b_layer_full_size(dbuf_lib, oracle_lib):
             so32 = db.state_offsets[t]
             assert_bits_equal(f32(st["m32"][so32:so32 + k]), m32[:k], f"m32 t{t}")
             assert_bits_equal(f32(st["v32"][so32:so32 + k]), v32[:k], f"v32 t{t}")
+
+
+def test_adamw8_every_group_size_in_one_launch(dbuf_lib, oracle_lib):
+    """Blocks of 16 to 8192 elements in one plan: threads per block 1, 16, 64,
+    128, 256 and 512 in the pipelined kernel, with more stages than SMs so that
+    one CTA moves between tensors (and named-barrier ranges) from stage to
+    stage; and the same plan through the register kernel (unaligned buffers)."""
+    specs = [
+        TensorSpec("s64x64", 768, 640, 64, qblock=(64, 64), quant="int8"),      # 256 threads/block
+        TensorSpec("s64x128", 512, 1024, 64, qblock=(64, 128), quant="int8"),   # 512
+        TensorSpec("s32x64", 640, 768, 32, qblock=(32, 64), quant="int8"),      # 128
+        TensorSpec("vec", 1000, 1, 1),
+        TensorSpec("s16x16", 400, 1280, 16, qblock=(16, 16), quant="int8"),     # 16
+        TensorSpec("s32x32", 704, 704, 32, qblock=(32, 32), quant="int8"),      # 64
+        TensorSpec("s1x16", 1024, 512, 1, qblock=(1, 16), quant="int8"),        # 1
+    ]
+    c = Case(oracle_lib, specs, 4, seed=9)
+    c.step(1, clip=True)
+    c.step(2)
+    c = Case(oracle_lib, specs, 3, seed=10, shift=1)
+    c.step(1)
