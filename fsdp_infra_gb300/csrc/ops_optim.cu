@@ -676,26 +676,6 @@ constexpr size_t kP8SmemBytes = size_t(kP8Stages) * kP8StageBytes + 1024 +
                                 2 * kP8Stages * 8 + 16 * kP8Warps * 8 +
                                 kP8MaxTensors * sizeof(P8Slot);
 
-// OR of `pred` over the `count` threads of named barrier `id` (a block group).
-__device__ __forceinline__ bool group_any(bool pred, int id, int count) {
-    int r;
-    asm volatile(
-        "{\n"
-        ".reg .pred p, q;\n"
-        "setp.ne.s32 p, %1, 0;\n"
-        "barrier.cta.red.or.pred q, %2, %3, p;\n"
-        "selp.s32 %0, 1, 0, q;\n"
-        "}\n"
-        : "=r"(r)
-        : "r"(int(pred)), "r"(id), "r"(count)
-        : "memory");
-    return r != 0;
-}
-
-__device__ __forceinline__ void group_sync(int id, int count) {
-    asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
-}
-
 // The block of stage item `it` that thread `tid` works on, and its scale index.
 struct P8Place {
     int bl, j, rb, kb, bi, bj;

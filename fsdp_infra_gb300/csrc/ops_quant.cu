@@ -284,23 +284,29 @@ __global__ void __launch_bounds__(kThreads)
 
 // ---------------------------------------------------------------------------
 // Pipelined tile kernel.  One 512-thread CTA per SM walks its tiles (item
-// blockIdx.x, blockIdx.x + gridDim.x, ...) through a ring of kPipeStages
-// shared-memory tile buffers.  One thread fetches a whole tile with a single
-// 2-D tensor-memory-access copy (cp.async.bulk.tensor, tensor map of that
-// tensor, zero fill past the tensor's edge) completing on the buffer's
-// mbarrier; all warps wait on it, pull the tile into registers (warp w holds
-// rows w, w+16, ...), and after the block-wide amax barrier the buffer is
-// refilled with the tile kPipeStages ahead while the codes are encoded and
-// stored.  With 3 buffers, two tiles stream in while one is encoded.
-// Every mbarrier wait is bounded: on expiry the CTA records DBUF_ETIMEOUT in
-// the plan's status word, waits (bounded again) for its own copies still in
-// flight, and returns.
+// blockIdx.x, blockIdx.x + gridDim.x, ...) in two groups of 8 warps that take
+// alternate tiles, so that one group's per-tile chain (wait, maxima, group
+// barrier, scale, encode) overlaps the other's.  Each group owns one tile
+// buffer: its phases are consumed by that group alone and strictly in order,
+// which a parity wait needs (with buffers shared round-robin between groups,
+// one group could run two phases ahead on a buffer and take a stale phase for
+// its own).  One thread fetches a whole tile with a single 2-D
+// tensor-memory-access copy (cp.async.bulk.tensor, tensor map of that tensor,
+// zero fill past the tensor's edge) completing on the buffer's mbarrier; the
+// group's warps pull the tile into registers (warp w of the group holds rows
+// w, w+8, ...), meet the maximum at the group's named barrier, and the
+// group's first thread refills the buffer with the group's next tile while
+// the codes are encoded and stored.  Every mbarrier
+// wait is bounded: a group decides a failed wait together at its barrier,
+// records DBUF_ETIMEOUT in the plan's status word and stops; after a CTA-wide
+// barrier thread 0 waits (bounded again) for copies still in flight.
 // ---------------------------------------------------------------------------
 constexpr int kPipeThreads = 512;
 constexpr int kPipeWarps = kPipeThreads / 32;
-constexpr int kPipeStages = 3;
+constexpr int kPipeGroupWarps = kPipeWarps / 2;     // warps per ping-pong group
+constexpr int kPipeStages = 2;   // one tile buffer per group
 constexpr int kPipeStageBytes = kPipeMaxRows * kPipeMaxCols * 4;
-constexpr int kPipeRowsPerWarp = kPipeMaxRows / kPipeWarps;
+constexpr int kPipeRowsPerWarp = kPipeMaxRows / kPipeGroupWarps;
 constexpr size_t kPipeSmemBytes = size_t(kPipeStages) * kPipeStageBytes + 1024 + 256;
 
 struct TmaMaps {
@@ -347,7 +353,7 @@ __device__ __forceinline__ void pipe_encode_store(const PipeTile &g, const float
     if (!dv.exact) {
 #pragma unroll
         for (int k = 0; k < kPipeRowsPerWarp; ++k) {
-            const int r = warp + k * kPipeWarps;
+            const int r = warp + k * kPipeGroupWarps;
             if (r < g.h && col_ok)
                 __stcs(reinterpret_cast<unsigned int *>(g.y + r * g.cols + 4 * lane),
                        encode4<Q, false>(v[k], dv));
@@ -355,7 +361,7 @@ __device__ __forceinline__ void pipe_encode_store(const PipeTile &g, const float
     } else {
 #pragma unroll
         for (int k = 0; k < kPipeRowsPerWarp; ++k) {
-            const int r = warp + k * kPipeWarps;
+            const int r = warp + k * kPipeGroupWarps;
             if (r < g.h && col_ok)
                 __stcs(reinterpret_cast<unsigned int *>(g.y + r * g.cols + 4 * lane),
                        encode4<Q, true>(v[k], dv));
@@ -372,32 +378,39 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
     uint64_t *bars = reinterpret_cast<uint64_t *>(stages + size_t(kPipeStages) * kPipeStageBytes);
-    float *sh_max = reinterpret_cast<float *>(bars + kPipeStages);  // [2][kPipeWarps]
+    float *sh_max = reinterpret_cast<float *>(bars + kPipeStages);  // [2 groups][2][kPipeGroupWarps]
+    int *last = reinterpret_cast<int *>(sh_max + 4 * kPipeGroupWarps);  // last tile issued per buffer
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int grp = warp / kPipeGroupWarps, gw = warp % kPipeGroupWarps;
+    const int gtid = tid - grp * kPipeGroupWarps * 32;   // thread index in the group
+    const int gbar = 1 + grp;                            // the group's named barrier
     const int G = gridDim.x;
     const float iq448 = __frcp_rn(448.0f), iq127 = __frcp_rn(127.0f);  // RN(1 / qmax)
 
     if (tid == 0) {
-        for (int s = 0; s < kPipeStages; ++s) mbar_init(&bars[s], 1);
+        for (int s = 0; s < kPipeStages; ++s) {
+            mbar_init(&bars[s], 1);
+            last[s] = -1;
+        }
         mbar_fence_init();
     }
     __syncthreads();
 
     // Prologue: the first kPipeStages tiles of this CTA.
-    int issued = 0;  // tiles of this CTA whose copies were issued
-    for (int s = 0; s < kPipeStages; ++s) {
-        const int i = blockIdx.x + s * G;
-        if (i >= nitems) break;
-        if (tid == 0) pipe_issue(pipe_tile(items[i], td, codes), maps, stages + s * kPipeStageBytes,
-                                 &bars[s]);
-        ++issued;
-    }
+    const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
+    if (tid == 0)
+        for (int s = 0; s < kPipeStages && s < mine; ++s) {
+            last[s] = s;  // before the copy, whose arrive releases it to the group
+            pipe_issue(pipe_tile(items[blockIdx.x + s * G], td, codes), maps,
+                       stages + s * kPipeStageBytes, &bars[s]);
+        }
 
-    int k = 0;  // index of the tile of this CTA being processed
-    bool failed = false;
-    for (int i = blockIdx.x; i < nitems; i += G, ++k) {
-        const int s = k % kPipeStages;
-        const uint32_t parity = uint32_t(k / kPipeStages) & 1u;
+    // Group grp takes this CTA's tiles k = grp, grp + 2, ..., all in buffer grp:
+    // tile k is that buffer's phase k / 2.
+    for (int k = grp; k < mine; k += 2) {
+        const int i = int(blockIdx.x) + k * G;
+        const int s = grp;
+        const uint32_t parity = uint32_t(k / 2) & 1u;
         const PipeTile g = pipe_tile(items[i], td, codes);
         const bool got = mbar_wait_bounded(&bars[s], parity);
 
@@ -407,43 +420,44 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         float amax = 0.0f;
 #pragma unroll
         for (int r8 = 0; r8 < kPipeRowsPerWarp; ++r8) {
-            const int r = warp + r8 * kPipeWarps;
+            const int r = gw + r8 * kPipeGroupWarps;
             v[r8] = (r < g.h && col_ok)
                         ? *reinterpret_cast<const float4 *>(st + r * g.qcols + 4 * lane)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
             amax = abs_max4(amax, v[r8]);
         }
         amax = warp_max(amax);
-        if (lane == 0) sh_max[(k & 1) * kPipeWarps + warp] = amax;
-        // Every thread has its rows in registers: the buffer may be refilled.
-        if (__syncthreads_or(!got)) {
-            failed = true;
+        float *slot = sh_max + (grp * 2 + ((k >> 1) & 1)) * kPipeGroupWarps;
+        if (lane == 0) slot[gw] = amax;
+        // Every thread of the group has its rows in registers: the buffer may be
+        // refilled.  The barrier also settles the group's verdict on the wait.
+        if (group_any(!got, gbar, kPipeGroupWarps * 32)) {
+            if (gtid == 0) atomicExch(status, DBUF_ETIMEOUT);
             break;
         }
-        const int inext = i + kPipeStages * G;
-        if (inext < nitems) {
-            if (tid == 0) pipe_issue(pipe_tile(items[inext], td, codes), maps,
-                                     stages + s * kPipeStageBytes, &bars[s]);
-            ++issued;
+        if (gtid == 0 && k + 2 < mine) {
+            last[s] = k + 2;
+            pipe_issue(pipe_tile(items[i + 2 * G], td, codes), maps, stages + s * kPipeStageBytes,
+                       &bars[s]);
         }
-        amax = warp_max(sh_max[(k & 1) * kPipeWarps + (lane % kPipeWarps)]);
+        amax = warp_max(slot[lane % kPipeGroupWarps]);
         if (g.quant == DBUF_QUANT_E4M3) {
             const float scale = block_scale_cr(amax, QParams<DBUF_QUANT_E4M3>::qmax, iq448);
-            pipe_encode_store<DBUF_QUANT_E4M3>(g, v, make_divisor(scale), warp, lane);
-            if (tid == 0) scales[g.scale_idx] = scale;
+            pipe_encode_store<DBUF_QUANT_E4M3>(g, v, make_divisor(scale), gw, lane);
+            if (gtid == 0) scales[g.scale_idx] = scale;
         } else {
             const float scale = block_scale_cr(amax, QParams<DBUF_QUANT_INT8>::qmax, iq127);
-            pipe_encode_store<DBUF_QUANT_INT8>(g, v, make_divisor(scale), warp, lane);
-            if (tid == 0) scales[g.scale_idx] = scale;
+            pipe_encode_store<DBUF_QUANT_INT8>(g, v, make_divisor(scale), gw, lane);
+            if (gtid == 0) scales[g.scale_idx] = scale;
         }
     }
-    if (failed && tid == 0) {
-        atomicExch(status, DBUF_ETIMEOUT);
-        // Copies of tiles k .. issued-1 may still be in flight into this CTA's
-        // shared memory: wait for them (bounded) before the CTA exits.
-        for (int j = k; j < issued; ++j)
-            (void)mbar_wait_bounded(&bars[j % kPipeStages], uint32_t(j / kPipeStages) & 1u);
-    }
+    // A copy issued for a tile that a failed group no longer takes may still be
+    // in flight into this CTA's shared memory: wait (bounded) for the last copy
+    // issued into each buffer before the CTA exits.
+    __syncthreads();
+    if (tid == 0)
+        for (int s = 0; s < kPipeStages; ++s)
+            if (last[s] >= 0) (void)mbar_wait_bounded(&bars[s], uint32_t(last[s] / 2) & 1u);
 }
 
 // Host: the tensor-map encoder, looked up once from the driver.

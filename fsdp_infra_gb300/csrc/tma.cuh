@@ -76,6 +76,26 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
 }
 
 
+// OR of `pred` over the `count` threads of named barrier `id` (a block group).
+__device__ __forceinline__ bool group_any(bool pred, int id, int count) {
+    int r;
+    asm volatile(
+        "{\n"
+        ".reg .pred p, q;\n"
+        "setp.ne.s32 p, %1, 0;\n"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n"
+        "selp.s32 %0, 1, 0, q;\n"
+        "}\n"
+        : "=r"(r)
+        : "r"(int(pred)), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void group_sync(int id, int count) {
+    asm volatile("barrier.cta.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // Host: a 2-D tensor map over a row-major fp32 or uint8 tensor (cols x rows,
 // row pitch cols elements) with a box_cols x box_rows box, zero fill outside
 // the tensor.  False when the encoder is missing or rejects the arguments.
