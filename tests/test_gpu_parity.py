@@ -2,7 +2,7 @@
 
 Bit-exact: layout, pack/unpack (with the fp32->bf16 RNE cast), scale/accumulate/
 zero, block-quantisation codes and scales.  Norms: within 1e-5 relative of the
-oracle's fp64 norms (the tolerance the benchmark spec fixes for the fp32 L2 norm).  Small
+oracle's fp64 norms (fp32 squares and sums against an fp64 reference).  Small
 workloads are compared over whole buffers, padding included (padding must stay
 exactly as it was).
 """
