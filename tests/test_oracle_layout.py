@@ -121,7 +121,7 @@ def test_naive_concatenation_is_rejected():
 
 
 def test_invariant_checker_catches_planted_mistakes(oracle_lib):
-    """A layout with a single field perturbed must fail the checker."""
+    """A layout with a single field perturbed must fail the layout checker."""
     w = workload("tiny")
     specs = w.groups[0].tensors
     p = _plan(oracle_lib, specs, w.m, None, w.align)
