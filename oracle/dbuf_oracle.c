@@ -12,13 +12,14 @@
  *           §4 RaggedShard format; §5 Planning algorithm (problem formulation,
  *           default tensor order, 3-case analysis); §5 DBuffer (group-level
  *           operators, zero-copy access); §6.3 8-bit Adam (block-wise quantisation
- *           of the local shard without communication).
+ *           of the local shard without communication); §6.3 Distributed Muon
+ *           (whole-matrix redistribution to a root and back, Algorithm 2).
  *  [FSDP-2] "PyTorch FSDP: Experiences on Scaling Fully Sharded Data Parallel",
  *           FlatParameter; native mixed precision; gradient accumulation;
  *           sharded gradient scaler; known limitations.
  *  [veScale-3] "veScale 深度技术分析", RaggedShard Placement (placement_types.py:
  *           flattened storage, local_units); OpDispatcher (ragged norm handler,
- *           found_inf handler).
+ *           found_inf handler, fused AdamW/SGD handler).
  *
  * Readings where the pages leave a step open are stated at each function.
  */
