@@ -210,8 +210,8 @@ def test_adamw8_dense7b_layer_full_size(dbuf_lib, oracle_lib):
 
 
 def test_adamw8_every_group_size_in_one_launch(dbuf_lib, oracle_lib):
-    """Blocks of 16 to 8192 elements in one plan: threads per block 1, 16, 64,
-    128, 256 and 512 in the pipelined kernel, with more stages than SMs so that
+    """Blocks of 16 to 8192 elements in one plan: threads per block 1, 8, 16,
+    64, 128, 256 and 512 in the pipelined kernel, two-row blocks included, with more stages than SMs so that
     one CTA moves between tensors (and named-barrier ranges) from stage to
     stage; and the same plan through the register kernel (unaligned buffers)."""
     specs = [
@@ -222,6 +222,11 @@ def test_adamw8_every_group_size_in_one_launch(dbuf_lib, oracle_lib):
         TensorSpec("s16x16", 400, 1280, 16, qblock=(16, 16), quant="int8"),     # 16
         TensorSpec("s32x32", 704, 704, 32, qblock=(32, 32), quant="int8"),      # 64
         TensorSpec("s1x16", 1024, 512, 1, qblock=(1, 16), quant="int8"),        # 1
+        # two-row blocks whose rows hold more units than the block has threads: a
+        # thread's units continue on the block's second row
+        TensorSpec("s2x64", 258, 640, 2, qblock=(2, 64), quant="int8"),         # 8
+        TensorSpec("s2x128", 130, 1152, 2, qblock=(2, 128), quant="int8"),      # 16
+        TensorSpec("s4x32", 100, 160, 4, qblock=(4, 32), quant="int8"),         # 8
     ]
     c = Case(oracle_lib, specs, 4, seed=9)
     c.step(1, clip=True)
