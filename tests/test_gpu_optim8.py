@@ -211,9 +211,10 @@ def test_adamw8_dense7b_layer_full_size(dbuf_lib, oracle_lib):
 
 def test_adamw8_every_group_size_in_one_launch(dbuf_lib, oracle_lib):
     """Blocks of 16 to 8192 elements in one plan: threads per block 1, 8, 16,
-    64, 128, 256 and 512 in the pipelined kernel, two-row blocks included, with more stages than SMs so that
-    one CTA moves between tensors (and named-barrier ranges) from stage to
-    stage; and the same plan through the register kernel (unaligned buffers)."""
+    32, 64, 128, 256 and 512 in the pipelined kernel, two-row blocks included,
+    with more stages than SMs so that one CTA moves between tensors (and
+    named-barrier ranges) from stage to stage; and the same plan through the
+    register kernel (unaligned buffers)."""
     specs = [
         TensorSpec("s64x64", 768, 640, 64, qblock=(64, 64), quant="int8"),      # 256 threads/block
         TensorSpec("s64x128", 512, 1024, 64, qblock=(64, 128), quant="int8"),   # 512
@@ -222,6 +223,8 @@ def test_adamw8_every_group_size_in_one_launch(dbuf_lib, oracle_lib):
         TensorSpec("s16x16", 400, 1280, 16, qblock=(16, 16), quant="int8"),     # 16
         TensorSpec("s32x32", 704, 704, 32, qblock=(32, 32), quant="int8"),      # 64
         TensorSpec("s1x16", 1024, 512, 1, qblock=(1, 16), quant="int8"),        # 1
+        TensorSpec("s16x32", 336, 416, 16, qblock=(16, 32), quant="int8"),      # 32
+        TensorSpec("s4x128", 36, 896, 4, qblock=(4, 128), quant="int8"),        # 32
         # two-row blocks whose rows hold more units than the block has threads: a
         # thread's units continue on the block's second row
         TensorSpec("s2x64", 258, 640, 2, qblock=(2, 64), quant="int8"),         # 8
