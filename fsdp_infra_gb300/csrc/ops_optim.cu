@@ -391,6 +391,24 @@ __device__ __forceinline__ void unit_update(const AdamScalars &s, float *params,
     store_c<W>(vc, e, cv);
 }
 
+// The codes of a unit of 4 from its new moments by the reciprocal-step
+// quotient (both scales in [2^-80, 2^100]), as in unit_update<4, false>.
+__device__ __forceinline__ void unit_codes_fast(const float (&m)[4], const float (&v)[4],
+                                                const Divisor &dm, const Divisor &dv, uint32_t &cm,
+                                                uint32_t &cv) {
+    const float2 mg = splat(kMagicRound);
+    const float2 qm01 = __fadd2_rn(quot2(make_float2(m[0], m[1]), dm), mg);
+    const float2 qm23 = __fadd2_rn(quot2(make_float2(m[2], m[3]), dm), mg);
+    cm = low_bytes(qm01.x, qm01.y, qm23.x, qm23.y);
+    float2 qv01 = quot2(make_float2(v[0], v[1]), dv);
+    float2 qv23 = quot2(make_float2(v[2], v[3]), dv);
+    qv01 = make_float2(fmaxf(qv01.x, 1.0f), fmaxf(qv01.y, 1.0f));
+    qv23 = make_float2(fmaxf(qv23.x, 1.0f), fmaxf(qv23.y, 1.0f));
+    qv01 = __fadd2_rn(__fadd2_rn(qv01, mg), splat(-1.0f));
+    qv23 = __fadd2_rn(__fadd2_rn(qv23, mg), splat(-1.0f));
+    cv = low_bytes(qv01.x, qv01.y, qv23.x, qv23.y);
+}
+
 // Walk of one lane over its units u = j, j + lanes, ... of a block with `upr`
 // units per row: (row, cu) advances by (dr, dc) with one carry.
 struct UnitWalk {
@@ -641,24 +659,35 @@ __global__ void __launch_bounds__(kThreads, 4)
 // whole quantisation blocks of one tensor holding kP8StageElems elements,
 // fetched with four 2-D tensor-map copies (p, g, m codes, v codes) into one of
 // two shared-memory buffers and completing on the buffer's "full" mbarrier.
-// Thread 0 issues the copies of stage k+2 into the buffer of stage k as soon
-// as every warp has released it (its "empty" mbarrier, one arrival per warp,
-// after the warp has its data in registers).  Every thread takes 16
+// The warp that releases the buffer of stage k last (a shared-memory count,
+// one acquire-release increment per warp once the warp has its data in
+// registers) issues the copies of stage k+2 into it, so that no warp waits
+// for the others to release.  Every thread takes 16
 // elements (four units of 4) of one block: it steps the moments, the block's
 // threads meet their maxima (integer max within a warp; across warps through
 // shared memory and a named barrier whose id range belongs to one group size),
 // and it stores the parameters and codes to HBM.  Per-tensor geometry sits in
 // a shared-memory table; the next stage's item and old scales are loaded one
 // iteration ahead.  Every wait is bounded: a block group decides a failed wait
-// together before its next barrier, records DBUF_ETIMEOUT and stops; thread 0
-// stops issuing on a failed wait but keeps taking part in its group, and
-// waits (bounded) for copies still in flight before the CTA exits.
+// together before its next barrier, records DBUF_ETIMEOUT and stops (a stage
+// that a stopped warp never releases is never refilled, so the others stop at
+// their next wait); thread 0 waits (bounded) for copies still in flight
+// before the CTA exits.
 // ---------------------------------------------------------------------------
 constexpr int kP8Warps = kP8ComputeWarps;
 constexpr int kP8Threads = kP8Warps * 32;
 constexpr int kP8U = kP8UnitsPerThread;
 constexpr int kP8StageBytes = kP8StageElems * 10;    // p, g (fp32) + m, v codes
 constexpr int kP8Stages = 2;
+
+__device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.cta.shared::cta.add.u32 %0, [%1], %2;"
+                 : "=r"(old)
+                 : "r"(smem_u32(p)), "r"(v)
+                 : "memory");
+    return old;
+}
 
 struct P8Maps {
     CUtensorMap map[kP8MaxTensors][4];  // p, g, m codes, v codes
@@ -718,10 +747,12 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
     uint64_t *full = reinterpret_cast<uint64_t *>(stages + size_t(kP8Stages) * kP8StageBytes);
-    uint64_t *empty = full + kP8Stages;
+    // per buffer: warps that have released it; then the number of stages issued
+    uint32_t *rel = reinterpret_cast<uint32_t *>(full + kP8Stages);
+    int *nissued = reinterpret_cast<int *>(rel + kP8Stages);
     // block maxima across warps: one row of slots per named barrier, so that a
     // slot is only ever shared by the warps of one group
-    float2 *red = reinterpret_cast<float2 *>(empty + kP8Stages);  // [16][kP8Warps]
+    float2 *red = reinterpret_cast<float2 *>(full + 2 * kP8Stages);  // [16][kP8Warps]
     P8Slot *slots = reinterpret_cast<P8Slot *>(red + 16 * kP8Warps);
     const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
     const int G = int(gridDim.x);
@@ -752,7 +783,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     if (tid == 0) {
         for (int st = 0; st < kP8Stages; ++st) {
             mbar_init(&full[st], 1);
-            mbar_init(&empty[st], kP8Warps);
+            rel[st] = 0;
         }
         mbar_fence_init();
     }
@@ -760,12 +791,13 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     const AdamScalars s = adam_scalars(hp, total_norm);
     const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
     if (mine == 0) return;
-    bool issuing = true;  // thread 0: still issuing copies
-    int issued = 0;
-    if (tid == 0)
+    if (tid == 0) {
+        int issued = 0;
         for (; issued < kP8Stages && issued < mine; ++issued)
             p8_issue(maps, slots, items[int(blockIdx.x) + issued * G],
                      stages + size_t(issued) * kP8StageBytes, &full[issued]);
+        *nissued = issued;
+    }
 
     P8Item cur = items[blockIdx.x];
     float ms_cur = 0.0f, vs_cur = 0.0f;
@@ -819,17 +851,16 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             cvw[u2] = *reinterpret_cast<const uint32_t *>(buf + kP8StageElems * 9 + so);
         }
         // the buffer may be refilled once every warp has its data in registers:
-        // thread 0 waits for all releases and issues stage k + kP8Stages into it
+        // the last warp to release it issues stage k + kP8Stages into it (the
+        // count is next used with that stage, whose copies follow the reset)
         __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[st]);
-        if (tid == 0 && issuing && k + kP8Stages < mine) {
-            if (!mbar_wait_bounded(&empty[st], uint32_t(k / kP8Stages) & 1u)) {
-                issuing = false;
-                atomicExch(status, DBUF_ETIMEOUT);
-            } else {
-                p8_issue(maps, slots, items[int(blockIdx.x) + (k + kP8Stages) * G],
+        if (lane == 0 && atom_add_acq_rel(&rel[st], 1u) == kP8Warps - 1) {
+            rel[st] = 0;
+            const int j = k + kP8Stages;
+            if (j < mine) {
+                p8_issue(maps, slots, items[int(blockIdx.x) + j * G],
                          stages + size_t(st) * kP8StageBytes, &full[st]);
-                ++issued;
+                *nissued = j + 1;
             }
         }
 
@@ -889,15 +920,45 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             const bool vzero = !(vs_new > 0.0f);
             const bool fast = s.fast && mamax <= 0x1p60f && vamax <= 0x1p60f;
             const bool exact = dm.exact || dv.exact;
+            // the common case decided once for the thread's 16 elements, so that
+            // their update chains share one basic block and interleave
+            bool all = fast && !exact;
 #pragma unroll
-            for (int u2 = 0; u2 < kP8U; ++u2) {
-                if (!valid[u2]) continue;
-                if (exact)
-                    unit_update<4, true>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv,
-                                         vzero, fast);
-                else
-                    unit_update<4, false>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm, dv,
-                                          vzero, fast);
+            for (int u2 = 0; u2 < kP8U; ++u2)
+#pragma unroll
+                for (int w = 0; w < 4; ++w)
+                    all = all && (!valid[u2] ||
+                                  (v[u2][w] >= 0x1p-60f && fabsf(m[u2][w]) >= 0x1p-60f));
+            if (all) {
+#pragma unroll
+                for (int u2 = 0; u2 < kP8U; ++u2)
+#pragma unroll
+                    for (int w = 0; w < 4; ++w)
+                        p[u2][w] = adam_param_cr(s, p[u2][w], m[u2][w], v[u2][w]);
+                uint32_t cm[kP8U], cv[kP8U];
+#pragma unroll
+                for (int u2 = 0; u2 < kP8U; ++u2)
+                    unit_codes_fast(m[u2], v[u2], dm, dv, cm[u2], cv[u2]);
+#pragma unroll
+                for (int u2 = 0; u2 < kP8U; ++u2) {
+                    if (!valid[u2]) continue;
+                    store_f<4>(params, e[u2], p[u2]);
+                    store_c<4>(mc, e[u2], cm[u2]);
+                    store_c<4>(vc, e[u2], cv[u2]);
+                }
+            } else {
+                // per unit: IEEE forms where a value leaves the range, exact quotients
+                // for scales outside [2^-80, 2^100]
+#pragma unroll
+                for (int u2 = 0; u2 < kP8U; ++u2) {
+                    if (!valid[u2]) continue;
+                    if (exact)
+                        unit_update<4, true>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm,
+                                             dv, vzero, fast);
+                    else
+                        unit_update<4, false>(s, params, mc, vc, e[u2], p[u2], m[u2], v[u2], dm,
+                                              dv, vzero, fast);
+                }
             }
             if (q.j == 0) {
                 ms[q.si] = ms_new;
@@ -908,9 +969,11 @@ __global__ void __launch_bounds__(kP8Threads, 1)
         ms_cur = ms_nxt;
         vs_cur = vs_nxt;
     }
+    __syncthreads();  // every warp has left the loop: the count of stages issued is final
     if (tid == 0) {
         // copies of the last stages issued may still be in flight: wait for them
-        // (bounded) before the CTA exits
+        // (bounded) before the CTA exits (stages are issued in order)
+        const int issued = *nissued;
         for (int j = (issued > kP8Stages ? issued - kP8Stages : 0); j < issued; ++j)
             (void)mbar_wait_bounded(&full[j % kP8Stages], uint32_t(j / kP8Stages) & 1u);
     }
