@@ -89,6 +89,52 @@ __device__ __forceinline__ float adam_param_cr(const AdamScalars &s, float p, fl
     return __fsub_rn(pd, __fmul_rn(s.step, div_cr(m, denom, rcp_cr(denom))));
 }
 
+// adam_moments on a pair: the products packed, each sum scalar (a packed
+// product may only feed a scalar, correctly rounded sum, never a packed one).
+__device__ __forceinline__ void adam_moments2(const AdamScalars &s, float g0, float g1, float &m0,
+                                              float &m1, float &v0, float &v1) {
+    const float2 g = __fmul2_rn(make_float2(g0, g1), make_float2(s.coef, s.coef));
+    const float2 a = __fmul2_rn(make_float2(s.beta1, s.beta1), make_float2(m0, m1));
+    const float2 b = __fmul2_rn(make_float2(s.omb1, s.omb1), g);
+    m0 = __fadd_rn(a.x, b.x);
+    m1 = __fadd_rn(a.y, b.y);
+    const float2 c = __fmul2_rn(make_float2(s.beta2, s.beta2), make_float2(v0, v1));
+    const float2 d = __fmul2_rn(__fmul2_rn(make_float2(s.omb2, s.omb2), g), g);
+    v0 = __fadd_rn(c.x, d.x);
+    v1 = __fadd_rn(c.y, d.y);
+}
+
+// adam_param_cr on a pair with the packed fp32x2 multiply, fused multiply-add
+// and add: per element the same IEEE operations in the same order.  No packed
+// multiply feeds a packed add here (each feeds a fused multiply-add), so the
+// compiler has nothing to contract; p * decay - step * q, the one place where
+// a product meets a sum, stays scalar.
+__device__ __forceinline__ float2 neg2(float2 a) { return make_float2(-a.x, -a.y); }
+
+__device__ __forceinline__ void adam_param_cr2(const AdamScalars &s, float &p0, float &p1, float m0,
+                                               float m1, float v0, float v1) {
+    const float2 v = make_float2(v0, v1), m = make_float2(m0, m1);
+    // v / bc2
+    const float2 ib = make_float2(s.ibc2, s.ibc2);
+    const float2 q1 = __fmul2_rn(v, ib);
+    const float2 a = __ffma2_rn(__ffma2_rn(q1, make_float2(-s.bc2, -s.bc2), v), ib, q1);
+    // its square root, plus eps
+    const float2 r = make_float2(rsqrt_approx(a.x), rsqrt_approx(a.y));
+    const float2 sq = __fmul2_rn(a, r);
+    const float2 h = __fmul2_rn(make_float2(0.5f, 0.5f), r);
+    const float2 root = __ffma2_rn(__ffma2_rn(neg2(sq), sq, a), h, sq);
+    const float2 den = __fadd2_rn(root, make_float2(s.eps, s.eps));
+    // its reciprocal, then m / den
+    const float2 nden = neg2(den), one = make_float2(1.0f, 1.0f);
+    float2 y = make_float2(rcp_approx(den.x), rcp_approx(den.y));
+    y = __ffma2_rn(__ffma2_rn(nden, y, one), y, y);
+    y = __ffma2_rn(__ffma2_rn(nden, y, one), y, y);
+    const float2 q2 = __fmul2_rn(m, y);
+    const float2 t = __ffma2_rn(__ffma2_rn(q2, nden, m), y, q2);
+    p0 = __fsub_rn(__fmul_rn(p0, s.decay), __fmul_rn(s.step, t.x));
+    p1 = __fsub_rn(__fmul_rn(p1, s.decay), __fmul_rn(s.step, t.y));
+}
+
 __device__ __forceinline__ void adam_elem(const AdamScalars &s, float &p, float g, float &m,
                                           float &v) {
     adam_moments(s, g, m, v);
@@ -800,6 +846,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     }
 
     P8Item cur = items[blockIdx.x];
+    P8Item nxt = mine > 1 ? items[int(blockIdx.x) + G] : cur;  // loaded a stage ahead
     float ms_cur = 0.0f, vs_cur = 0.0f;
     {
         const P8Place q = p8_place(slots[cur.slot], cur, tid);
@@ -810,11 +857,12 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     }
     for (int k = 0; k < mine; ++k) {
         const int st = k % kP8Stages;
-        // the next item and its old scales, one iteration ahead
-        P8Item nxt = cur;
+        // the item after next (its load has a stage to land), and the next
+        // item's old scales, one iteration ahead
+        P8Item nxt2 = nxt;
+        if (k + 2 < mine) nxt2 = items[int(blockIdx.x) + (k + 2) * G];
         float ms_nxt = 0.0f, vs_nxt = 0.0f;
         if (k + 1 < mine) {
-            nxt = items[int(blockIdx.x) + (k + 1) * G];
             const P8Place qn = p8_place(slots[nxt.slot], nxt, tid);
             if (qn.block) {
                 ms_nxt = ms[qn.si];
@@ -876,7 +924,9 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             m[u2][0] = m01.x; m[u2][1] = m01.y; m[u2][2] = m23.x; m[u2][3] = m23.y;
             v[u2][0] = v01.x; v[u2][1] = v01.y; v[u2][2] = v23.x; v[u2][3] = v23.y;
 #pragma unroll
-            for (int w = 0; w < 4; ++w) adam_moments(s, gw[u2][w], m[u2][w], v[u2][w]);
+            for (int w = 0; w < 4; w += 2)
+                adam_moments2(s, gw[u2][w], gw[u2][w + 1], m[u2][w], m[u2][w + 1], v[u2][w],
+                              v[u2][w + 1]);
             if (valid[u2]) {
 #pragma unroll
                 for (int w = 0; w < 4; ++w) {
@@ -933,8 +983,9 @@ __global__ void __launch_bounds__(kP8Threads, 1)
 #pragma unroll
                 for (int u2 = 0; u2 < kP8U; ++u2)
 #pragma unroll
-                    for (int w = 0; w < 4; ++w)
-                        p[u2][w] = adam_param_cr(s, p[u2][w], m[u2][w], v[u2][w]);
+                    for (int w = 0; w < 4; w += 2)
+                        adam_param_cr2(s, p[u2][w], p[u2][w + 1], m[u2][w], m[u2][w + 1],
+                                       v[u2][w], v[u2][w + 1]);
                 uint32_t cm[kP8U], cv[kP8U];
 #pragma unroll
                 for (int u2 = 0; u2 < kP8U; ++u2)
@@ -966,6 +1017,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             }
         }
         cur = nxt;
+        nxt = nxt2;
         ms_cur = ms_nxt;
         vs_cur = vs_nxt;
     }
