@@ -89,6 +89,20 @@ __device__ __forceinline__ float adam_param_cr(const AdamScalars &s, float p, fl
     return __fsub_rn(pd, __fmul_rn(s.step, div_cr(m, denom, rcp_cr(denom))));
 }
 
+// Three-input maximum (a NaN input is ignored, as by fmaxf) and minimum (a NaN
+// input gives NaN) of sm_100+.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
+__device__ __forceinline__ float fmin3_nan(float a, float b, float c) {
+    float r;
+    asm("min.NaN.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 // adam_moments on a pair: the products packed, each sum scalar (a packed
 // product may only feed a scalar, correctly rounded sum, never a packed one).
 __device__ __forceinline__ void adam_moments2(const AdamScalars &s, float g0, float g1, float &m0,
@@ -879,6 +893,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
         int64_t e[kP8U];
         bool valid[kP8U];
         float mamax = 0.0f, vamax = 0.0f;
+        float mmin = __int_as_float(0x7F800000), vmin = __int_as_float(0x7F800000);
         uint32_t cmw[kP8U], cvw[kP8U];
         float gw[kP8U][4];
 #pragma unroll
@@ -928,13 +943,17 @@ __global__ void __launch_bounds__(kP8Threads, 1)
                 adam_moments2(s, gw[u2][w], gw[u2][w + 1], m[u2][w], m[u2][w + 1], v[u2][w],
                               v[u2][w + 1]);
             if (valid[u2]) {
-#pragma unroll
-                for (int w = 0; w < 4; ++w) {
-                    mamax = fmaxf(mamax, fabsf(m[u2][w]));
-                    vamax = fmaxf(vamax, v[u2][w]);
-                }
+                const float a0 = fabsf(m[u2][0]), a1 = fabsf(m[u2][1]);
+                const float a2 = fabsf(m[u2][2]), a3 = fabsf(m[u2][3]);
+                mamax = fmax3(fmax3(mamax, a0, a1), a2, a3);
+                vamax = fmax3(fmax3(vamax, v[u2][0], v[u2][1]), v[u2][2], v[u2][3]);
+                mmin = fmin3_nan(fmin3_nan(mmin, a0, a1), a2, a3);
+                vmin = fmin3_nan(fmin3_nan(vmin, v[u2][0], v[u2][1]), v[u2][2], v[u2][3]);
             }
         }
+        // every |m| and v of the thread's units inside the range of the exact forms
+        // (false for a NaN)
+        const bool inrange = mmin >= 0x1p-60f && vmin >= 0x1p-60f;
 
         // block maxima and the group's verdict on the wait
         bool failed;
@@ -972,14 +991,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
             const bool exact = dm.exact || dv.exact;
             // the common case decided once for the thread's 16 elements, so that
             // their update chains share one basic block and interleave
-            bool all = fast && !exact;
-#pragma unroll
-            for (int u2 = 0; u2 < kP8U; ++u2)
-#pragma unroll
-                for (int w = 0; w < 4; ++w)
-                    all = all && (!valid[u2] ||
-                                  (v[u2][w] >= 0x1p-60f && fabsf(m[u2][w]) >= 0x1p-60f));
-            if (all) {
+            if (fast && !exact && inrange) {
 #pragma unroll
                 for (int u2 = 0; u2 < kP8U; ++u2)
 #pragma unroll
