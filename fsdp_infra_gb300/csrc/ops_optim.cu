@@ -44,14 +44,19 @@ struct AdamScalars {
     bool fast;   // bc2 and eps inside the range of the correctly rounded forms
 };
 
+// The clipping coefficient min(1, max_norm / (total_norm + 1e-6)), 1 without clipping.
+__device__ __forceinline__ float clip_coef(const dbuf_adamw_hparams &hp, const float *total_norm) {
+    if (hp.max_norm > 0.0f && total_norm) {
+        const float c = __fdiv_rn(hp.max_norm, __fadd_rn(*total_norm, 1e-6f));
+        return c < 1.0f ? c : 1.0f;
+    }
+    return 1.0f;
+}
+
 __device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp,
                                                     const float *total_norm) {
     AdamScalars s;
-    s.coef = 1.0f;
-    if (hp.max_norm > 0.0f && total_norm) {
-        const float c = __fdiv_rn(hp.max_norm, __fadd_rn(*total_norm, 1e-6f));
-        s.coef = c < 1.0f ? c : 1.0f;
-    }
+    s.coef = clip_coef(hp, total_norm);
     s.decay = __fsub_rn(1.0f, __fmul_rn(hp.lr, hp.weight_decay));
     s.step = __fdiv_rn(hp.lr, hp.bias_correction1);
     s.beta1 = hp.beta1;
@@ -62,6 +67,35 @@ __device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp
     s.eps = hp.eps;
     s.ibc2 = __frcp_rn(s.bc2);
     s.i127 = __frcp_rn(127.0f);
+    s.fast = s.bc2 >= 0x1p-40f && s.bc2 <= 1.0f && s.eps >= 0.0f && s.eps <= 0x1p40f;
+    return s;
+}
+
+// The same scalars but coef, computed on the host for a kernel that takes them
+// as parameters (operands from the constant bank instead of registers).  Each
+// operation is one IEEE single-precision operation rounded to nearest, as on
+// the device; a volatile result keeps every product and quotient rounded on
+// its own (no contraction into a fused multiply-add).
+AdamScalars host_scalars(const dbuf_adamw_hparams &hp) {
+    AdamScalars s;
+    volatile float t;
+    s.coef = 1.0f;
+    t = hp.lr * hp.weight_decay;
+    s.decay = 1.0f - t;
+    t = hp.lr / hp.bias_correction1;
+    s.step = t;
+    s.beta1 = hp.beta1;
+    s.beta2 = hp.beta2;
+    t = 1.0f - hp.beta1;
+    s.omb1 = t;
+    t = 1.0f - hp.beta2;
+    s.omb2 = t;
+    s.bc2 = hp.bias_correction2;
+    s.eps = hp.eps;
+    t = 1.0f / s.bc2;
+    s.ibc2 = t;
+    t = 1.0f / 127.0f;
+    s.i127 = t;
     s.fast = s.bc2 >= 0x1p-40f && s.bc2 <= 1.0f && s.eps >= 0.0f && s.eps <= 0x1p40f;
     return s;
 }
@@ -801,8 +835,8 @@ __global__ void __launch_bounds__(kP8Threads, 1)
                        int nitems, const TensorDesc *__restrict__ td, float *__restrict__ params,
                        uint8_t *__restrict__ mc, uint8_t *__restrict__ vc, float *__restrict__ ms,
                        float *__restrict__ vs, const dbuf_adamw_hparams hp,
-                       const float *__restrict__ total_norm, const int32_t *__restrict__ nonfinite,
-                       int32_t *__restrict__ status) {
+                       const AdamScalars hs, const float *__restrict__ total_norm,
+                       const int32_t *__restrict__ nonfinite, int32_t *__restrict__ status) {
     extern __shared__ unsigned char smem_raw[];
     char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
@@ -848,7 +882,8 @@ __global__ void __launch_bounds__(kP8Threads, 1)
         mbar_fence_init();
     }
     __syncthreads();
-    const AdamScalars s = adam_scalars(hp, total_norm);
+    AdamScalars s = hs;
+    s.coef = clip_coef(hp, total_norm);
     const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
     if (mine == 0) return;
     if (tid == 0) {
@@ -1092,7 +1127,7 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
         const int g = n < p->dev.num_sms ? n : p->dev.num_sms;
         adamw8_pipe_kernel<<<g, kP8Threads, kP8SmemBytes, st>>>(
             maps, p->dev.p8_items, n, p->dev.tensors, params, m_codes, v_codes, m_scales, v_scales,
-            hp, total_norm, nonfinite, p->dev.status);
+            hp, host_scalars(hp), total_norm, nonfinite, p->dev.status);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }
