@@ -92,7 +92,8 @@ class Case:
                 g[int(o):int(o) + s.numel:7] = 0.0
         return g
 
-    def step(self, step, clip=False, skip=False):
+    def step(self, step, clip=False, skip=False, hp=None):
+        hp = HP if hp is None else hp
         g = self.grad()
         gd = _dev(g, self.shift)
         _, wt, _ = self.ol.norm_nonfinite(self.op, g)
@@ -101,12 +102,12 @@ class Case:
         self.flag.fill_(1 if skip else 0)
         max_norm = 0.5 * total32 if clip else 0.0
         self.db.adamw8_step(self.d["p"], gd, self.state, step=step, max_norm=max_norm,
-                            total_norm=self.norm, nonfinite=self.flag, **HP)
-        b1, b2 = HP["betas"]
+                            total_norm=self.norm, nonfinite=self.flag, **hp)
+        b1, b2 = hp["betas"]
         h = self.h
         self.ol.adamw8(self.op, self.specs, h["p"], g, h["mc"], h["vc"], h["ms"], h["vs"],
-                       h["m32"], h["v32"], lr=HP["lr"], beta1=b1, beta2=b2, eps=HP["eps"],
-                       weight_decay=HP["weight_decay"], bc1=float(np.float32(1 - b1 ** step)),
+                       h["m32"], h["v32"], lr=hp["lr"], beta1=b1, beta2=b2, eps=hp["eps"],
+                       weight_decay=hp["weight_decay"], bc1=float(np.float32(1 - b1 ** step)),
                        bc2=float(np.float32(1 - b2 ** step)), max_norm=max_norm,
                        total_norm=total32, nonfinite=1 if skip else 0)
         torch.cuda.synchronize()
@@ -236,3 +237,25 @@ def test_adamw8_every_group_size_in_one_launch(dbuf_lib, oracle_lib):
     c.step(2)
     c = Case(oracle_lib, specs, 3, seed=10, shift=1)
     c.step(1)
+
+
+@pytest.mark.parametrize("hp,steps", [
+    (dict(lr=3e-4, betas=(0.8, 0.999), eps=1e-6, weight_decay=0.0), (1, 2, 3)),
+    (dict(lr=1e-2, betas=(0.95, 0.99), eps=0.0, weight_decay=0.5), (1, 7)),
+    # late steps: both bias corrections near 1
+    (dict(lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1), (500, 5000)),
+])
+def test_adamw8_hyperparameters(dbuf_lib, oracle_lib, hp, steps):
+    """Other betas, eps (0 included), weight decay and late steps, on block
+    shapes of the pipelined kernel (its step scalars are computed on the host)
+    and on those of the register kernel, against the oracle."""
+    specs = [
+        TensorSpec("s32x32", 160, 224, 32, qblock=(32, 32), quant="int8"),
+        TensorSpec("s1x128", 40, 384, 1, qblock=(1, 128), quant="int8"),
+        TensorSpec("vec", 300, 1, 1),
+        TensorSpec("s128", 256, 136, 128, qblock=(128, 128), quant="int8"),
+    ]
+    c = Case(oracle_lib, specs, 4, seed=11)
+    for i, st in enumerate(steps):
+        c.step(st, clip=(i % 2 == 1), hp=hp)
+
