@@ -103,14 +103,15 @@ static_assert(sizeof(Piece) == 32, "Piece layout");
 // Rb) x [bj0, bj0 + K) of tensor `tensor` (tensor-map slot `slot`), 4096
 // elements; Rb and K follow from the tensor's block shape.
 struct P8Item {
-    int32_t slot;
+    int32_t slot;    // within its launch: the plan's p8 tensor index mod kP8MaxTensors
     int32_t tensor;
     int32_t bi0;
     int32_t bj0;
 };
 static_assert(sizeof(P8Item) == 16, "P8Item layout");
 
-constexpr int kP8MaxTensors = 16;      // tensors with tensor maps per launch (4 maps each)
+constexpr int kP8MaxTensors = 16;      // tensors with tensor maps per launch (4 maps each);
+                                       // a group with more takes one launch per 16
 constexpr int kP8ComputeWarps = 16;    // compute warps per CTA of the pipelined kernel
 constexpr int kP8UnitsPerThread = 4;   // units of 4 elements per compute thread and stage
 constexpr int kP8StageElems = kP8ComputeWarps * 32 * 4 * kP8UnitsPerThread;  // elements per stage
@@ -207,6 +208,7 @@ struct dbuf_plan {
     std::vector<dbuf::Piece> pieces;
     std::vector<dbuf::P8Item> p8_items;
     std::vector<int32_t> p8_tensors;     // slot -> tensor id
+    std::vector<size_t> p8_item_start;   // [slots + 1]: first p8 item of each slot
     size_t n_opt_rest = 0;               // opt_items[0, n_opt_rest): tensors without p8 items
     std::vector<int64_t> state_offsets;  // [n], -1 for quantised tensors
     int64_t n_state = 0;

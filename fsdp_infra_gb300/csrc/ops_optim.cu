@@ -783,6 +783,9 @@ __device__ __forceinline__ uint32_t atom_add_acq_rel(uint32_t *p, uint32_t v) {
     return old;
 }
 
+// The tensor maps of one launch: the plan's p8 tensors b * kP8MaxTensors ..
+// b * kP8MaxTensors + nslots - 1 for launch b, whose items carry their slot
+// within the launch.
 struct P8Maps {
     CUtensorMap map[kP8MaxTensors][4];  // p, g, m codes, v codes
     int32_t tensor[kP8MaxTensors];      // slot -> tensor
@@ -1107,27 +1110,42 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
     const uintptr_t bits = reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(grads) |
                            reinterpret_cast<uintptr_t>(m_codes) | reinterpret_cast<uintptr_t>(v_codes);
     bool pipe = !p->p8_items.empty() && (bits & 15) == 0;
-    P8Maps maps;
-    maps.nslots = int32_t(p->p8_tensors.size());
-    for (size_t slot = 0; pipe && slot < p->p8_tensors.size(); ++slot) {
-        maps.tensor[slot] = p->p8_tensors[slot];
-        const TensorDesc &d = p->tdesc[p->p8_tensors[slot]];
-        const int qe = d.qrows * d.qcols, nblk = kP8StageElems / qe;
-        const int K = std::min(256 / d.qcols, nblk), bw = K * d.qcols, bh = (nblk / K) * d.qrows;
-        pipe = encode_map_2d(&maps.map[slot][0], true, params + d.buf_off, d.cols, d.rows, bw, bh) &&
-               encode_map_2d(&maps.map[slot][1], true, const_cast<float *>(grads) + d.buf_off,
-                             d.cols, d.rows, bw, bh) &&
-               encode_map_2d(&maps.map[slot][2], false, m_codes + d.buf_off, d.cols, d.rows, bw, bh) &&
-               encode_map_2d(&maps.map[slot][3], false, v_codes + d.buf_off, d.cols, d.rows, bw, bh);
+    // one launch per kP8MaxTensors tensors; every map is encoded before the first
+    // launch, so that a tensor the encoder rejects sends all of them to the
+    // register kernel
+    const size_t nslot = p->p8_tensors.size();
+    std::vector<P8Maps> batches;
+    for (size_t b0 = 0; pipe && b0 < nslot; b0 += kP8MaxTensors) {
+        P8Maps maps;
+        maps.nslots = int32_t(std::min<size_t>(kP8MaxTensors, nslot - b0));
+        for (int slot = 0; pipe && slot < maps.nslots; ++slot) {
+            const int32_t t = p->p8_tensors[b0 + slot];
+            maps.tensor[slot] = t;
+            const TensorDesc &d = p->tdesc[t];
+            const int qe = d.qrows * d.qcols, nblk = kP8StageElems / qe;
+            const int K = std::min(256 / d.qcols, nblk), bw = K * d.qcols, bh = (nblk / K) * d.qrows;
+            pipe = encode_map_2d(&maps.map[slot][0], true, params + d.buf_off, d.cols, d.rows, bw,
+                                 bh) &&
+                   encode_map_2d(&maps.map[slot][1], true, const_cast<float *>(grads) + d.buf_off,
+                                 d.cols, d.rows, bw, bh) &&
+                   encode_map_2d(&maps.map[slot][2], false, m_codes + d.buf_off, d.cols, d.rows,
+                                 bw, bh) &&
+                   encode_map_2d(&maps.map[slot][3], false, v_codes + d.buf_off, d.cols, d.rows,
+                                 bw, bh);
+        }
+        batches.push_back(maps);
     }
     const size_t n_items = pipe ? p->n_opt_rest : p->opt_items.size();
     const size_t grid = p->opt_plain.size() + n_items;
-    if (pipe) {
-        const int n = int(p->p8_items.size());
+    for (size_t b = 0; pipe && b < batches.size(); ++b) {
+        const size_t b0 = b * kP8MaxTensors;
+        const size_t i0 = p->p8_item_start[b0], i1 = p->p8_item_start[b0 + batches[b].nslots];
+        const int n = int(i1 - i0);
+        if (n == 0) continue;
         const int g = n < p->dev.num_sms ? n : p->dev.num_sms;
         adamw8_pipe_kernel<<<g, kP8Threads, kP8SmemBytes, st>>>(
-            maps, p->dev.p8_items, n, p->dev.tensors, params, m_codes, v_codes, m_scales, v_scales,
-            hp, host_scalars(hp), total_norm, nonfinite, p->dev.status);
+            batches[b], p->dev.p8_items + i0, n, p->dev.tensors, params, m_codes, v_codes,
+            m_scales, v_scales, hp, host_scalars(hp), total_norm, nonfinite, p->dev.status);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;
     }

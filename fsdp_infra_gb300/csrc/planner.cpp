@@ -232,6 +232,7 @@ void build_tables(dbuf_plan_t *p) {
     p->opt_plain.clear();
     p->p8_items.clear();
     p->p8_tensors.clear();
+    p->p8_item_start.assign(1, 0);
     std::vector<dbuf::OptItem> p8_opt;  // register-kernel items of p8 tensors (the fallback)
     p->state_offsets.assign(n, -1);
     int64_t s_off = 0, st_off = 0;
@@ -285,14 +286,14 @@ void build_tables(dbuf_plan_t *p) {
                                 be <= dbuf::kP8StageElems && be >= 4 * dbuf::kP8UnitsPerThread &&
                                 s.cols % 16 == 0 &&
                                 d.buf_off % 16 == 0 && s.rows < (int64_t(1) << 31) &&
-                                s.cols < (int64_t(1) << 31) &&
-                                p->p8_tensors.size() < size_t(dbuf::kP8MaxTensors);
+                                s.cols < (int64_t(1) << 31);
                 std::vector<dbuf::OptItem> &dst = p8 ? p8_opt : p->opt_items;
                 for (int64_t b = 0; b < nb; b += per)
                     dst.push_back(dbuf::OptItem{t, int32_t(b / d.nbc), int32_t(b % d.nbc),
                                                 int16_t(std::min(per, nb - b)), int16_t(lanes)});
                 if (p8) {
-                    const int32_t slot = int32_t(p->p8_tensors.size());
+                    // the slot within its launch of at most kP8MaxTensors tensors
+                    const int32_t slot = int32_t(p->p8_tensors.size() % dbuf::kP8MaxTensors);
                     p->p8_tensors.push_back(t);
                     const int64_t nblk = dbuf::kP8StageElems / be;
                     const int64_t K = std::min<int64_t>(256 / d.qcols, nblk);
@@ -301,6 +302,7 @@ void build_tables(dbuf_plan_t *p) {
                         for (int64_t bj = 0; bj < d.nbc; bj += K)
                             p->p8_items.push_back(
                                 dbuf::P8Item{slot, t, int32_t(bi), int32_t(bj)});
+                    p->p8_item_start.push_back(p->p8_items.size());
                 }
             }
             if (d.qrows == 1) {

@@ -259,3 +259,22 @@ def test_adamw8_hyperparameters(dbuf_lib, oracle_lib, hp, steps):
     for i, st in enumerate(steps):
         c.step(st, clip=(i % 2 == 1), hp=hp)
 
+
+
+def test_adamw8_more_tensors_than_one_launch_holds(dbuf_lib, oracle_lib):
+    """41 quantised tensors of the pipelined kernel (three launches of at most 16
+    tensors each, shapes and block shapes changing across the batch boundaries)
+    with vectors between them, against the oracle; then the same plan through
+    the register kernel (unaligned buffers)."""
+    specs = []
+    for i in range(41):
+        qb = [(32, 32), (1, 128), (16, 64)][i % 3]
+        rows = qb[0] * (2 + i % 5) + (7 if qb[0] == 1 else 0)
+        specs.append(TensorSpec(f"w{i}", rows, 128 * (1 + i % 3), qb[0], qblock=qb, quant="int8"))
+        if i % 7 == 3:
+            specs.append(TensorSpec(f"b{i}", 96 + i, 1, 1))
+    c = Case(oracle_lib, specs, 4, seed=12)
+    c.step(1, clip=True)
+    c.step(2)
+    c = Case(oracle_lib, specs, 4, seed=13, shift=1)
+    c.step(1)
