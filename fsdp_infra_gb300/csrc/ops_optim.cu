@@ -760,9 +760,13 @@ __global__ void __launch_bounds__(kThreads, 4)
 // elements (four units of 4) of one block: it steps the moments, the block's
 // threads meet their maxima (integer max within a warp; across warps through
 // shared memory and a named barrier whose id range belongs to one group size),
-// and it stores the parameters and codes to HBM.  Per-tensor geometry sits in
-// a shared-memory table; the next stage's item and old scales are loaded one
-// iteration ahead.  Every wait is bounded: a block group decides a failed wait
+// and it updates the parameters and stores them and the codes to HBM.  A
+// thread whose 16 |m| and v all lie in the exact forms' range (the common
+// case) takes one branch for all of them, so that their update chains
+// interleave, on packed fp32x2 instructions.  Per-tensor geometry sits in a
+// shared-memory table; stage items are loaded two iterations ahead and old
+// scales one.  A launch takes the tensors of at most kP8MaxTensors tensor-map
+// slots.  Every wait is bounded: a block group decides a failed wait
 // together before its next barrier, records DBUF_ETIMEOUT and stops (a stage
 // that a stopped warp never releases is never refilled, so the others stop at
 // their next wait); thread 0 waits (bounded) for copies still in flight
