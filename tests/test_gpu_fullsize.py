@@ -133,3 +133,96 @@ def test_mixed_group_full_size(dbuf_lib, oracle_lib, oracle_plans):
     by_size = sorted(range(n), key=lambda t: specs[t].numel)
     sample = sorted(set(rng.sample(range(n), 48) + by_size[:4] + by_size[-4:]))
     sampled_group_parity(oracle_lib, oracle_plans("mixed", 0), w, 0, sample)
+
+
+def test_tensor_beyond_32bit_offsets(dbuf_lib, oracle_lib):
+    """One tensor of 2,149,580,800 elements (131200 x 16384, 128x128 E4M3 blocks)
+    after a small vector, m=2: element offsets and indices past 2^31 in every
+    operator of the step.  The layout against the oracle's plan; pack, unpack,
+    scale/accumulate/zero and block quantisation bit for bit on sampled block
+    rows (the first, the two on either side of the shard bound, the last); the
+    norm of the whole tensor against the oracle's, taken in 1 GB pieces; the
+    non-finite flag for one inf planted in the last element."""
+    from fsdp_infra_gb300 import DBuffer, dbuf
+    from workloads.configs import TensorSpec
+    R, C, B = 131200, 16384, 128
+    specs = [TensorSpec("lead", 1000, 1, 1),
+             TensorSpec("huge", R, C, B, qblock=(B, B), quant="e4m3")]
+    m, scale = 2, 0.5
+    op = oracle_lib.plan_specs(specs, m, None, 16)
+    db = DBuffer(specs, m, None, 16).upload()
+    assert db.S == op.S and db.total == op.total
+    assert db.offsets == [int(x) for x in op.offsets]
+    assert db.shard_bounds == [int(x) for x in op.bounds]
+    lo = db.offsets[1]
+    n = specs[1].numel
+    assert lo + n > 2 ** 31
+    # the shard bound falls between two block rows of the large tensor
+    cut = (db.S - lo) // C
+    assert 0 < cut < R and (db.S - lo) % (B * C) == 0
+    block_rows = sorted({0, cut // B - 1, cut // B, R // B - 1})
+
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(2024)
+    lead = torch.randn(1000, 1, generator=gen, device=DEV) * 0.02
+    huge = torch.randn(R, C, generator=gen, device=DEV) * 0.02
+    buf16 = torch.zeros(db.total, dtype=torch.bfloat16, device=DEV)
+    db.pack_cast([lead, huge], buf16)
+    dst = [torch.empty(1000, 1, dtype=torch.bfloat16, device=DEV),
+           torch.empty(R, C, dtype=torch.bfloat16, device=DEV)]
+    db.unpack(buf16, dst)
+    grad = torch.randn(db.total, generator=gen, device=DEV) * 1e-3
+    acc = torch.randn(db.total, generator=gen, device=DEV) * 1e-3
+    rows = [(b * B, (b + 1) * B) for b in block_rows]
+    g_rows = [f32(grad[lo + r0 * C:lo + r1 * C]).copy() for r0, r1 in rows]
+    a_rows = [f32(acc[lo + r0 * C:lo + r1 * C]).copy() for r0, r1 in rows]
+
+    norms, tot, flag = db.norm_nonfinite(grad)
+    torch.cuda.synchronize()
+    # the oracle's norms: the vector whole, the large tensor in 2^28-element pieces
+    # (sums of squares in fp64, recombined)
+    sq = [float(oracle_lib.norm_nonfinite(oracle_lib.plan_specs([specs[0]], 1, None, 1),
+                                          f32(grad[:1000]).copy())[0][0]) ** 2, 0.0]
+    piece = 1 << 28
+    for s0 in range(0, n, piece):
+        k = min(piece, n - s0)
+        sp = oracle_lib.plan_specs([TensorSpec("piece", k, 1, 1)], 1, None, 1)
+        nn, _, wf = oracle_lib.norm_nonfinite(sp, f32(grad[lo + s0:lo + s0 + k]))
+        assert wf == 0
+        sq[1] += float(nn[0]) ** 2
+    want = np.sqrt(np.array(sq))
+    assert int(flag.item()) == 0
+    assert_norms_close(f32(norms), tot.item(), want, math.sqrt(sum(sq)), what="2^31+ norms")
+
+    db.scale_accum_zero(grad, acc, scale)
+    codes, scales = db.block_quant(acc)
+    torch.cuda.synchronize()
+    so = int(oracle_lib.scale_offsets(specs)[0][1])
+    nbc = C // B
+    for (r0, r1), g_h, a_h in zip(rows, g_rows, a_rows):
+        sub = TensorSpec("rows", r1 - r0, C, B, qblock=(B, B), quant="e4m3")
+        sp = oracle_lib.plan_specs([sub], 1, None, 1)
+        k = sub.numel
+        base = lo + r0 * C
+        want16 = np.zeros(k, np.uint16)
+        oracle_lib.pack(sp, [f32(huge[r0:r1]).reshape(-1)], want16)
+        assert_bits_equal(bf16_bits(buf16[base:base + k]), want16, f"pack rows {r0}")
+        wd = np.zeros(k, np.uint16)
+        oracle_lib.unpack(sp, want16, [wd])
+        assert_bits_equal(bf16_bits(dst[1][r0:r1]).reshape(-1), wd, f"unpack rows {r0}")
+        oracle_lib.scale_accum_zero(sp, g_h, a_h, scale)
+        assert_bits_equal(f32(acc[base:base + k]), a_h, f"accumulate rows {r0}")
+        assert_bits_equal(f32(grad[base:base + k]), g_h, f"zero rows {r0}")
+        wc = np.zeros(k, np.uint8)
+        ws = oracle_lib.block_quant(sp, [sub], a_h, wc)
+        b = r0 // B
+        assert_bits_equal(f32(scales[so + b * nbc:so + (b + 1) * nbc]), ws[:nbc], f"scales rows {r0}")
+        assert_bits_equal(codes[base:base + k].cpu().numpy(), wc, f"codes rows {r0}")
+
+    grad[lo + n - 1] = float("inf")
+    _, _, flag = db.norm_nonfinite(grad)
+    assert int(flag.item()) == 1
+    assert dbuf.dbuf_device_status(db.handle) == 0
+    db.close()
+    del lead, huge, buf16, dst, grad, acc, codes, scales
+    torch.cuda.empty_cache()
