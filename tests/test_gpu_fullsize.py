@@ -226,3 +226,113 @@ def test_tensor_beyond_32bit_offsets(dbuf_lib, oracle_lib):
     db.close()
     del lead, huge, buf16, dst, grad, acc, codes, scales
     torch.cuda.empty_cache()
+
+
+def test_next_rows_beyond_32bit_offsets(dbuf_lib, oracle_lib):
+    """The next rows past 32-bit offsets, on one 131200 x 16384 tensor
+    (2,149,580,800 elements) after a vector, m=2: 8-bit AdamW with 32x32 INT8
+    blocks (the pipelined kernel) and fp32 AdamW bit for bit against the oracle
+    on sampled block rows (both ends, either side of the shard bound), with
+    clipping; gather of the tensor from the two shard slices and scatter back,
+    compared with the flat buffer on the same rows."""
+    from fsdp_infra_gb300 import DBuffer, dbuf
+    from workloads.configs import TensorSpec
+    R, C, B = 131200, 16384, 32
+    specs = [TensorSpec("lead", 1000, 1, 1),
+             TensorSpec("huge", R, C, B, qblock=(B, B), quant="int8")]
+    m = 2
+    op = oracle_lib.plan_specs(specs, m, None, 16)
+    db = DBuffer(specs, m, None, 16).upload()
+    assert db.offsets == [int(x) for x in op.offsets] and db.total == op.total
+    lo, n = db.offsets[1], specs[1].numel
+    assert lo + n > 2 ** 31
+    cut = (db.S - lo) // C
+    assert 0 < cut < R and (db.S - lo) % (B * C) == 0
+    block_rows = sorted({0, cut // B - 1, cut // B, R // B - 1})
+    rows = [(b * B, (b + 1) * B) for b in block_rows]
+    nbc = C // B
+    hp = dict(lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
+    b1, b2 = hp["betas"]
+    step, max_norm, total = 3, 0.5, 0.75
+    bc1, bc2 = float(np.float32(1 - b1 ** step)), float(np.float32(1 - b2 ** step))
+    okw = dict(lr=hp["lr"], beta1=b1, beta2=b2, eps=hp["eps"], weight_decay=hp["weight_decay"],
+               bc1=bc1, bc2=bc2, max_norm=max_norm, total_norm=total)
+
+    gen = torch.Generator(device=DEV)
+    gen.manual_seed(31)
+    p = torch.randn(db.total, generator=gen, device=DEV) * 0.02
+    g = torch.randn(db.total, generator=gen, device=DEV) * 1e-3
+    st = db.new_adamw8_state()
+    st["m_codes"].copy_(torch.randint(0, 256, (db.total,), generator=gen, device=DEV,
+                                      dtype=torch.int32).to(torch.uint8))
+    st["v_codes"].copy_(torch.randint(0, 256, (db.total,), generator=gen, device=DEV,
+                                      dtype=torch.int32).to(torch.uint8))
+    st["m_scales"].uniform_(1e-7, 1e-5, generator=gen)
+    st["v_scales"].uniform_(1e-12, 1e-9, generator=gen)
+    so = int(oracle_lib.scale_offsets(specs)[0][1])
+    before = []
+    for r0, r1 in rows:
+        a, e = lo + r0 * C, lo + r1 * C
+        s0, s1 = so + (r0 // B) * nbc, so + (r1 // B) * nbc
+        before.append({k: x for k, x in (
+            ("p", f32(p[a:e]).copy()), ("g", f32(g[a:e]).copy()),
+            ("mc", st["m_codes"][a:e].cpu().numpy().copy()),
+            ("vc", st["v_codes"][a:e].cpu().numpy().copy()),
+            ("ms", f32(st["m_scales"][s0:s1]).copy()), ("vs", f32(st["v_scales"][s0:s1]).copy()))})
+    tn = torch.tensor([total], dtype=torch.float32, device=DEV)
+    db.adamw8_step(p, g, st, step=step, max_norm=max_norm, total_norm=tn, **hp)
+    torch.cuda.synchronize()
+    for (r0, r1), h in zip(rows, before):
+        sub = TensorSpec("rows", r1 - r0, C, B, qblock=(B, B), quant="int8")
+        sp = oracle_lib.plan_specs([sub], 1, None, 1)
+        z = np.zeros(1, np.float32)
+        oracle_lib.adamw8(sp, [sub], h["p"], h["g"], h["mc"], h["vc"], h["ms"], h["vs"], z,
+                          z.copy(), **okw)
+        a, e = lo + r0 * C, lo + r1 * C
+        s0, s1 = so + (r0 // B) * nbc, so + (r1 // B) * nbc
+        assert_bits_equal(f32(p[a:e]), h["p"], f"adamw8 params rows {r0}")
+        assert np.array_equal(st["m_codes"][a:e].cpu().numpy(), h["mc"]), f"m codes rows {r0}"
+        assert np.array_equal(st["v_codes"][a:e].cpu().numpy(), h["vc"]), f"v codes rows {r0}"
+        assert_bits_equal(f32(st["m_scales"][s0:s1]), h["ms"], f"m scales rows {r0}")
+        assert_bits_equal(f32(st["v_scales"][s0:s1]), h["vs"], f"v scales rows {r0}")
+    del st
+    torch.cuda.empty_cache()
+
+    # fp32 AdamW on the same buffers
+    mom = torch.randn(db.total, generator=gen, device=DEV) * 1e-4
+    vel = torch.rand(db.total, generator=gen, device=DEV) * 1e-8
+    before = []
+    for r0, r1 in rows:
+        a, e = lo + r0 * C, lo + r1 * C
+        before.append([f32(x[a:e]).copy() for x in (p, g, mom, vel)])
+    db.adamw_step(p, g, mom, vel, step=step, max_norm=max_norm, total_norm=tn, **hp)
+    torch.cuda.synchronize()
+    for (r0, r1), (hp_, hg, hm, hv) in zip(rows, before):
+        sp = oracle_lib.plan_specs([TensorSpec("rows", r1 - r0, C, B)], 1, None, 1)
+        oracle_lib.adamw(sp, hp_, hg, hm, hv, **okw)
+        a, e = lo + r0 * C, lo + r1 * C
+        assert_bits_equal(f32(p[a:e]), hp_, f"adamw params rows {r0}")
+        assert_bits_equal(f32(mom[a:e]), hm, f"adamw m rows {r0}")
+        assert_bits_equal(f32(vel[a:e]), hv, f"adamw v rows {r0}")
+    del mom, vel
+    torch.cuda.empty_cache()
+
+    # gather from the two shard slices of p, scatter back into zeroed slices of g
+    bnd = db.shard_bounds
+    shards = [p[bnd[k]:bnd[k + 1]] for k in range(m)]
+    full = torch.empty(R, C, dtype=torch.float32, device=DEV)
+    db.gather(shards, [None, full])
+    g.zero_()
+    back = [g[bnd[k]:bnd[k + 1]] for k in range(m)]
+    db.scatter([None, full], back)
+    torch.cuda.synchronize()
+    for r0, r1 in rows:
+        a, e = lo + r0 * C, lo + r1 * C
+        want = f32(p[a:e])
+        assert_bits_equal(f32(full[r0:r1]).reshape(-1), want, f"gather rows {r0}")
+        assert_bits_equal(f32(g[a:e]), want, f"scatter rows {r0}")
+    assert float(g[:1000].abs().max().item()) == 0.0  # the skipped vector stays untouched
+    assert dbuf.dbuf_device_status(db.handle) == 0
+    db.close()
+    del p, g, full, shards, back
+    torch.cuda.empty_cache()
