@@ -120,8 +120,8 @@ def test_naive_concatenation_is_rejected():
     assert any(e.startswith("(iii)") for e in errs)
 
 
-def test_invariant_checker_catches_planted_mistakes(oracle_lib):
-    """A layout with a single field perturbed must fail the layout checker."""
+def test_invariant_check_catches_planted_mistakes(oracle_lib):
+    """A layout with a single field perturbed must fail the invariant check."""
     w = workload("tiny")
     specs = w.groups[0].tensors
     p = _plan(oracle_lib, specs, w.m, None, w.align)
