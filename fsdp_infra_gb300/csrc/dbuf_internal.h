@@ -124,7 +124,7 @@ constexpr int64_t kOptItemElems = 16384;
 
 constexpr int kPipeMaxRows = 128;
 constexpr int kPipeMaxCols = 128;
-constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch
+constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch; more tensors take more launches
 
 struct DeviceTables {
     TensorDesc *tensors = nullptr;
@@ -202,7 +202,8 @@ struct dbuf_plan {
     std::vector<dbuf::RowItem> row_items;
     std::vector<dbuf::QItem> tile_items;
     std::vector<dbuf::TileItem> pipe_items;
-    std::vector<int32_t> pipe_tensors;  // slot -> tensor id
+    std::vector<int32_t> pipe_tensors;  // plan slot -> tensor id (launch slot = plan slot % 32)
+    std::vector<size_t> pipe_item_start;  // [slots + 1]: first pipelined tile of each slot
     std::vector<dbuf::OptItem> opt_items;
     std::vector<int32_t> opt_plain;      // chunk ids of tensors without quantisation
     std::vector<dbuf::Piece> pieces;

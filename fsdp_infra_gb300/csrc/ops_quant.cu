@@ -27,6 +27,7 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "quant_math.cuh"
@@ -503,9 +504,10 @@ namespace {
 
 // Tensor maps of the pipelined tensors of `p` over the buffer `buf` (one 2-D
 // map per tensor: columns x rows, row pitch cols*4 bytes, box qcols x qrows).
-bool encode_maps(const dbuf_plan_t *p, const float *buf, TmaMaps *maps) {
-    for (size_t slot = 0; slot < p->pipe_tensors.size(); ++slot) {
-        const TensorDesc &d = p->tdesc[p->pipe_tensors[slot]];
+// The maps of the plan's pipelined tensors b0 .. b0 + count - 1 (one launch).
+bool encode_maps(const dbuf_plan_t *p, const float *buf, TmaMaps *maps, size_t b0, size_t count) {
+    for (size_t slot = 0; slot < count; ++slot) {
+        const TensorDesc &d = p->tdesc[p->pipe_tensors[b0 + slot]];
         if (!encode_map_2d(&maps->map[slot], true, const_cast<float *>(buf + d.buf_off), d.cols,
                            d.rows, d.qcols, d.qrows))
             return false;
@@ -521,15 +523,30 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
     // Pipelined tiles need 16-byte aligned rows: a 16-byte-aligned fp32 buffer
     // and 4-byte-aligned codes (the plan checked the offsets and widths).
     bool pipe_ok = !p->pipe_items.empty() && aligned_mod(buf, 16) && aligned_mod(codes, 4);
-    TmaMaps maps;
-    if (pipe_ok) pipe_ok = encode_maps(p, buf, &maps);
+    // one launch per kPipeMaxTensors tensors; every map is encoded before the
+    // first launch, so that a map the encoder rejects sends all tiles to the
+    // register-tile kernel
+    const size_t nslot = p->pipe_tensors.size();
+    std::vector<TmaMaps> batches;
+    for (size_t b0 = 0; pipe_ok && b0 < nslot; b0 += kPipeMaxTensors) {
+        batches.emplace_back();
+        pipe_ok = encode_maps(p, buf, &batches.back(), b0,
+                              std::min<size_t>(kPipeMaxTensors, nslot - b0));
+    }
     if (pipe_ok) {
-        const int n = int(p->pipe_items.size());
-        const int grid = n < p->dev.num_sms ? n : p->dev.num_sms;
-        quant_pipe_kernel<<<grid, kPipeThreads, kPipeSmemBytes, st>>>(
-            maps, p->dev.pipe_items, n, p->dev.tensors, codes, scales, p->dev.status);
-        cudaError_t e = cudaGetLastError();
-        if (e != cudaSuccess) return e;
+        for (size_t b = 0; b < batches.size(); ++b) {
+            const size_t b0 = b * kPipeMaxTensors;
+            const size_t i0 = p->pipe_item_start[b0];
+            const size_t i1 = p->pipe_item_start[std::min(nslot, b0 + kPipeMaxTensors)];
+            const int n = int(i1 - i0);
+            if (n == 0) continue;
+            const int grid = n < p->dev.num_sms ? n : p->dev.num_sms;
+            quant_pipe_kernel<<<grid, kPipeThreads, kPipeSmemBytes, st>>>(
+                batches[b], p->dev.pipe_items + i0, n, p->dev.tensors, codes, scales,
+                p->dev.status);
+            cudaError_t e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+        }
     } else if (!p->pipe_items.empty()) {
         quant_tile_pipe_list_kernel<<<unsigned(p->pipe_items.size()), kTileThreads, 0, st>>>(
             p->dev.pipe_items, p->dev.tensors, buf, codes, scales);

@@ -228,6 +228,7 @@ void build_tables(dbuf_plan_t *p) {
     p->tile_items.clear();
     p->pipe_items.clear();
     p->pipe_tensors.clear();
+    p->pipe_item_start.assign(1, 0);
     p->opt_items.clear();
     p->opt_plain.clear();
     p->p8_items.clear();
@@ -313,13 +314,14 @@ void build_tables(dbuf_plan_t *p) {
             } else {
                 // Tiles a 2-D tensor map can fetch (rows and tile widths multiples of
                 // 16 bytes at a 16-byte-aligned tensor offset) go to the pipelined
-                // kernel, for the first kPipeMaxTensors such tensors; the rest to the
+                // kernel, which takes kPipeMaxTensors tensors per launch (an item
+                // carries its tensor's slot within the launch); the rest to the
                 // register-tile kernel.
                 const bool pipe = d.qrows <= dbuf::kPipeMaxRows && d.qcols <= dbuf::kPipeMaxCols &&
                                   d.qcols % 4 == 0 && s.cols % 4 == 0 && d.buf_off % 4 == 0 &&
-                                  s.rows < (int64_t(1) << 31) && s.cols < (int64_t(1) << 31) &&
-                                  p->pipe_tensors.size() < size_t(dbuf::kPipeMaxTensors);
-                const int32_t slot = pipe ? int32_t(p->pipe_tensors.size()) : -1;
+                                  s.rows < (int64_t(1) << 31) && s.cols < (int64_t(1) << 31);
+                const int32_t slot =
+                    pipe ? int32_t(p->pipe_tensors.size() % dbuf::kPipeMaxTensors) : -1;
                 if (pipe) p->pipe_tensors.push_back(t);
                 for (int64_t b = 0; b < nb; ++b) {
                     if (pipe)
@@ -328,6 +330,7 @@ void build_tables(dbuf_plan_t *p) {
                     else
                         p->tile_items.push_back(QItem{b, t, 1});
                 }
+                if (pipe) p->pipe_item_start.push_back(p->pipe_items.size());
             }
             s_off += nb;
         }

@@ -415,3 +415,27 @@ def test_quant_unaligned_buffers_and_status(lib, oracle_lib):
         assert_bits_equal(f32(scales), want_s, f"scales shift {fshift},{cshift}")
         assert_bits_equal(codes.cpu().numpy(), want_c, f"codes shift {fshift},{cshift}")
     assert lib.dbuf_device_status(db.handle) == 0
+
+
+def test_quant_more_tensors_than_one_launch_holds(lib, oracle_lib):
+    """75 tensors of the pipelined quantisation kernel (three launches of at most
+    32 tensors, block shapes 128x128, 64x128 and 32x32 in E4M3 and INT8 changing
+    across the batch boundaries, ragged edges) with vectors between them; every
+    operator against the oracle on whole buffers."""
+    from workloads.configs import TensorSpec
+    specs = []
+    for i in range(75):
+        qb = [(128, 128), (64, 128), (32, 32)][i % 3]
+        quant = "e4m3" if i % 2 == 0 else "int8"
+        rows = qb[0] * (1 + i % 3) + (5 if i % 4 == 1 else 0)
+        cols = 128 * (1 + i % 2) + (64 if i % 5 == 2 else 0)
+        specs.append(TensorSpec(f"w{i}", rows, cols, qb[0], qblock=qb, quant=quant))
+        if i % 9 == 4:
+            specs.append(TensorSpec(f"n{i}", 64 + i, 1, 1))
+    gen = torch.Generator().manual_seed(17)
+    ps = [torch.randn(s.rows, s.cols, generator=gen) * 0.02 for s in specs]
+    full_group_parity(oracle_lib, specs, 4, None, 16,
+                      param_fn=lambda t: ps[t],
+                      grad_fn=lambda t, step: torch.randn(specs[t].rows, specs[t].cols,
+                                                          generator=gen) * 1e-3,
+                      grad_dtype=torch.float32, scale=0.25)
