@@ -201,12 +201,17 @@ class Stack:
         self.bytes_per_step = sum(self.op_bytes.values())
         # pack, unpack, scale_accum_zero, norm (per-chunk partials + finalise) and one
         # quantisation launch per kind of block present (tiles, row blocks).
+        # one launch per DBuffer for each of pack_cast, unpack, scale_accum_zero
+        # and norm_nonfinite, plus the quantisation kernels: one launch per 32
+        # tile-quantised tensors (the tensor maps one launch carries) and one for
+        # row blocks
         self.launches_per_step = 0
         for d in self.dbufs:
             spec = d["kind"]["spec"]
-            qkinds = {("tile" if (s.qblock[0] or s.rows) > 1 else "row")
-                      for s in spec.tensors if s.quant and s.numel}
-            self.launches_per_step += 5 + len(qkinds)
+            q = [s for s in spec.tensors if s.quant and s.numel]
+            tiles = sum(1 for s in q if (s.qblock[0] or s.rows) > 1)
+            rows = len(q) - tiles
+            self.launches_per_step += 4 + (tiles + 31) // 32 + (1 if rows else 0)
 
     def run_op(self, op):
         """One operator alone over every DBuffer of the step, launched back to back."""
@@ -722,8 +727,13 @@ def run_adamw8(stack, args, world, peak, barrier):
         out = db.norm_nonfinite(g32)
         qe = sum(spec.numel for spec in g8.tensors if spec.quant)
         pe = sum(spec.numel for spec in g8.tensors if not spec.quant)
+        # launches: the pipelined kernel once per 16 quantised tensors (the tensor
+        # maps one launch carries), the register kernel once for the rest
+        nq = sum(1 for spec in g8.tensors if spec.quant and spec.numel)
+        rest = any(spec.numel and not spec.quant for spec in g8.tensors)
         kinds[gi] = {"db": db, "p": p32, "g": g32, "state": db.new_adamw8_state(), "out": out,
-                     "bytes": 16 * qe + 28 * pe + 16 * db.n_scales}
+                     "bytes": 16 * qe + 28 * pe + 16 * db.n_scales,
+                     "launches": (nq + 15) // 16 + (1 if rest else 0)}
     order = [d["kind"]["gi"] for d in stack.dbufs]
 
     def step(i):
@@ -765,7 +775,7 @@ def run_adamw8(stack, args, world, peak, barrier):
             "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
             "frac_of_peak": round(gbs / world / peak, 4),
             "bytes_per_step": nbytes, "flat_elements_per_step": elems,
-            "launches_per_step": len(order),
+            "launches_per_step": sum(kinds[gi]["launches"] for gi in order),
             "traffic_layer_launch": _traffic_for("adamw8"),
             "algorithmic_layer_launch": kinds[0]["bytes"]}
 
