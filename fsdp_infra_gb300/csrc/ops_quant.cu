@@ -305,10 +305,16 @@ __global__ void __launch_bounds__(kThreads)
 constexpr int kPipeThreads = 512;
 constexpr int kPipeWarps = kPipeThreads / 32;
 constexpr int kPipeGroupWarps = kPipeWarps / 2;     // warps per ping-pong group
-constexpr int kPipeStages = 2;   // one tile buffer per group
-constexpr int kPipeStageBytes = kPipeMaxRows * kPipeMaxCols * 4;
+// Each group owns a ring of three half-tile buffers: a tile's two halves (rows
+// [0, hr) and [hr, 2 hr), hr = ceil(qrows / 2)) are the group's halves 2t and
+// 2t + 1, half h lands in the group's buffer h % 3, so that while the group
+// works on tile t the first half of tile t + 1 is in flight and the rest
+// follows as soon as tile t is in registers (1.5 tiles in flight per group).
+constexpr int kPipeHalves = 3;
+constexpr int kPipeBuffers = 2 * kPipeHalves;
+constexpr int kPipeHalfBytes = (kPipeMaxRows / 2) * kPipeMaxCols * 4;
 constexpr int kPipeRowsPerWarp = kPipeMaxRows / kPipeGroupWarps;
-constexpr size_t kPipeSmemBytes = size_t(kPipeStages) * kPipeStageBytes + 1024 + 256;
+constexpr size_t kPipeSmemBytes = size_t(kPipeBuffers) * kPipeHalfBytes + 1024 + 256;
 
 struct TmaMaps {
     CUtensorMap map[kPipeMaxTensors];
@@ -318,7 +324,7 @@ struct PipeTile {
     uint8_t *y;
     int64_t cols;
     int64_t scale_idx;
-    int h, w, quant, qrows, qcols, slot, x0, y0;
+    int h, w, quant, qrows, qcols, slot, x0, y0, hr;
 };
 
 __device__ __forceinline__ PipeTile pipe_tile(const TileItem &it, const TensorDesc *__restrict__ td,
@@ -337,14 +343,16 @@ __device__ __forceinline__ PipeTile pipe_tile(const TileItem &it, const TensorDe
     g.slot = it.slot;
     g.x0 = int(c0);
     g.y0 = int(r0);
+    g.hr = (d.qrows + 1) / 2;
     return g;
 }
 
-// One thread: expect the full box (edge tiles are zero-filled) and fetch it.
-__device__ __forceinline__ void pipe_issue(const PipeTile &g, const TmaMaps &maps, char *stage,
-                                           uint64_t *bar) {
-    mbar_arrive_expect_tx(bar, uint32_t(g.qrows) * uint32_t(g.qcols) * 4u);
-    tma_load_2d(stage, &maps.map[g.slot], g.x0, g.y0, bar);
+// One thread: expect half e of the tile's box (hr rows; edges are zero-filled)
+// and fetch it.
+__device__ __forceinline__ void pipe_issue(const PipeTile &g, const TmaMaps &maps, int e,
+                                           char *stage, uint64_t *bar) {
+    mbar_arrive_expect_tx(bar, uint32_t(g.hr) * uint32_t(g.qcols) * 4u);
+    tma_load_2d(stage, &maps.map[g.slot], g.x0, g.y0 + e * g.hr, bar);
 }
 
 template <int Q>
@@ -378,9 +386,9 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // tensor copies land at 1024-byte-aligned buffers
     char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                             ~uintptr_t(1023));
-    uint64_t *bars = reinterpret_cast<uint64_t *>(stages + size_t(kPipeStages) * kPipeStageBytes);
-    float *sh_max = reinterpret_cast<float *>(bars + kPipeStages);  // [2 groups][2][kPipeGroupWarps]
-    int *last = reinterpret_cast<int *>(sh_max + 4 * kPipeGroupWarps);  // last tile issued per buffer
+    uint64_t *bars = reinterpret_cast<uint64_t *>(stages + size_t(kPipeBuffers) * kPipeHalfBytes);
+    float *sh_max = reinterpret_cast<float *>(bars + kPipeBuffers);  // [2 groups][2][kPipeGroupWarps]
+    int *last = reinterpret_cast<int *>(sh_max + 4 * kPipeGroupWarps);  // last half issued per buffer
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int grp = warp / kPipeGroupWarps, gw = warp % kPipeGroupWarps;
     const int gtid = tid - grp * kPipeGroupWarps * 32;   // thread index in the group
@@ -389,57 +397,66 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     const float iq448 = __frcp_rn(448.0f), iq127 = __frcp_rn(127.0f);  // RN(1 / qmax)
 
     if (tid == 0) {
-        for (int s = 0; s < kPipeStages; ++s) {
-            mbar_init(&bars[s], 1);
-            last[s] = -1;
+        for (int b = 0; b < kPipeBuffers; ++b) {
+            mbar_init(&bars[b], 1);
+            last[b] = -1;
         }
         mbar_fence_init();
     }
     __syncthreads();
 
-    // Prologue: the first kPipeStages tiles of this CTA.
+    // Group grp takes this CTA's tiles k = grp, grp + 2, ...: its t-th tile is
+    // k = 2t + grp, whose halves are the group's halves 2t and 2t + 1.
     const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
-    if (tid == 0)
-        for (int s = 0; s < kPipeStages && s < mine; ++s) {
-            last[s] = s;  // before the copy, whose arrive releases it to the group
-            pipe_issue(pipe_tile(items[blockIdx.x + s * G], td, codes), maps,
-                       stages + s * kPipeStageBytes, &bars[s]);
-        }
+    const int ntiles = (mine - grp + 1) / 2;
+    auto issue_half = [&](int h) {  // the group's first thread: half h into buffer h % 3
+        const int t = h >> 1, e = h & 1;
+        if (t >= ntiles) return;
+        const int b = grp * kPipeHalves + h % kPipeHalves;
+        last[b] = h;  // before the copy, whose arrive releases it to the group
+        pipe_issue(pipe_tile(items[int(blockIdx.x) + (2 * t + grp) * G], td, codes), maps, e,
+                   stages + size_t(b) * kPipeHalfBytes, &bars[b]);
+    };
+    if (gtid == 0)
+        for (int h = 0; h < kPipeHalves; ++h) issue_half(h);
 
-    // Group grp takes this CTA's tiles k = grp, grp + 2, ..., all in buffer grp:
-    // tile k is that buffer's phase k / 2.
-    for (int k = grp; k < mine; k += 2) {
-        const int i = int(blockIdx.x) + k * G;
-        const int s = grp;
-        const uint32_t parity = uint32_t(k / 2) & 1u;
+    for (int t = 0; t < ntiles; ++t) {
+        const int i = int(blockIdx.x) + (2 * t + grp) * G;
         const PipeTile g = pipe_tile(items[i], td, codes);
-        const bool got = mbar_wait_bounded(&bars[s], parity);
+        const int h0 = 2 * t, h1 = 2 * t + 1;
+        const int b0 = grp * kPipeHalves + h0 % kPipeHalves;
+        const int b1 = grp * kPipeHalves + h1 % kPipeHalves;
+        const bool got0 = mbar_wait_bounded(&bars[b0], uint32_t(h0 / kPipeHalves) & 1u);
+        const bool got = got0 && mbar_wait_bounded(&bars[b1], uint32_t(h1 / kPipeHalves) & 1u);
 
-        const float *st = reinterpret_cast<const float *>(stages + s * kPipeStageBytes);
+        const float *st0 = reinterpret_cast<const float *>(stages + size_t(b0) * kPipeHalfBytes);
+        const float *st1 = reinterpret_cast<const float *>(stages + size_t(b1) * kPipeHalfBytes);
         const bool col_ok = 4 * lane < g.w;
         float4 v[kPipeRowsPerWarp];
         float amax = 0.0f;
 #pragma unroll
         for (int r8 = 0; r8 < kPipeRowsPerWarp; ++r8) {
             const int r = gw + r8 * kPipeGroupWarps;
+            const bool second = r >= g.hr;
+            const float *st = second ? st1 : st0;
+            const int lr = second ? r - g.hr : r;
             v[r8] = (r < g.h && col_ok)
-                        ? *reinterpret_cast<const float4 *>(st + r * g.qcols + 4 * lane)
+                        ? *reinterpret_cast<const float4 *>(st + lr * g.qcols + 4 * lane)
                         : make_float4(0.f, 0.f, 0.f, 0.f);
             amax = abs_max4(amax, v[r8]);
         }
         amax = warp_max(amax);
-        float *slot = sh_max + (grp * 2 + ((k >> 1) & 1)) * kPipeGroupWarps;
+        float *slot = sh_max + (grp * 2 + (t & 1)) * kPipeGroupWarps;
         if (lane == 0) slot[gw] = amax;
-        // Every thread of the group has its rows in registers: the buffer may be
-        // refilled.  The barrier also settles the group's verdict on the wait.
+        // Every thread of the group has its rows in registers: both halves may be
+        // refilled.  The barrier also settles the group's verdict on the waits.
         if (group_any(!got, gbar, kPipeGroupWarps * 32)) {
             if (gtid == 0) atomicExch(status, DBUF_ETIMEOUT);
             break;
         }
-        if (gtid == 0 && k + 2 < mine) {
-            last[s] = k + 2;
-            pipe_issue(pipe_tile(items[i + 2 * G], td, codes), maps, stages + s * kPipeStageBytes,
-                       &bars[s]);
+        if (gtid == 0) {
+            issue_half(h0 + kPipeHalves);  // the second half of tile t + 1, into b0
+            issue_half(h1 + kPipeHalves);  // the first half of tile t + 2, into b1
         }
         amax = warp_max(slot[lane % kPipeGroupWarps]);
         if (g.quant == DBUF_QUANT_E4M3) {
@@ -457,8 +474,8 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     // issued into each buffer before the CTA exits.
     __syncthreads();
     if (tid == 0)
-        for (int s = 0; s < kPipeStages; ++s)
-            if (last[s] >= 0) (void)mbar_wait_bounded(&bars[s], uint32_t(last[s] / 2) & 1u);
+        for (int b = 0; b < kPipeBuffers; ++b)
+            if (last[b] >= 0) (void)mbar_wait_bounded(&bars[b], uint32_t(last[b] / kPipeHalves) & 1u);
 }
 
 // Host: the tensor-map encoder, looked up once from the driver.
@@ -509,7 +526,7 @@ bool encode_maps(const dbuf_plan_t *p, const float *buf, TmaMaps *maps, size_t b
     for (size_t slot = 0; slot < count; ++slot) {
         const TensorDesc &d = p->tdesc[p->pipe_tensors[b0 + slot]];
         if (!encode_map_2d(&maps->map[slot], true, const_cast<float *>(buf + d.buf_off), d.cols,
-                           d.rows, d.qcols, d.qrows))
+                           d.rows, d.qcols, (d.qrows + 1) / 2))
             return false;
     }
     return true;
