@@ -151,4 +151,31 @@ __device__ __forceinline__ bool aligned16(const void *a, const void *b) {
     return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
 }
 
+// Programmatic dependent launch.  A kernel launched with launch_pdl may be
+// scheduled while the previous kernel of its stream is still running; it must
+// call pdl_enter before its first access to global memory: the wait returns once
+// that kernel has completed and its writes are visible (at once for a kernel
+// launched the ordinary way), and the trigger then lets the next kernel be
+// scheduled in turn.  What overlaps is only launch and CTA scheduling.
+__device__ __forceinline__ void pdl_enter() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                       cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
 }  // namespace dbuf

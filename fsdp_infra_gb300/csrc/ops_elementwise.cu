@@ -43,6 +43,7 @@ template <int SRC, int DST>
 __global__ void __launch_bounds__(kThreads)
     pack_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                 const void *const *__restrict__ src, char *__restrict__ buf) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x];
     const char *s = static_cast<const char *>(src[c.tensor]) + c.off * elem_bytes<SRC>();
     char *d = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<DST>();
@@ -53,6 +54,7 @@ template <int SRC, int DST>
 __global__ void __launch_bounds__(kThreads)
     unpack_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                   const char *__restrict__ buf, void *const *__restrict__ dst) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x];
     const char *s = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<SRC>();
     char *d = static_cast<char *>(dst[c.tensor]) + c.off * elem_bytes<DST>();
@@ -64,6 +66,7 @@ template <int GDT>
 __global__ void __launch_bounds__(kThreads)
     sac_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                char *__restrict__ grad, float *__restrict__ acc, float scale) {
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x];
     const int64_t base = td[c.tensor].buf_off + c.off;
     char *g = grad + base * elem_bytes<GDT>();
@@ -114,17 +117,18 @@ __global__ void __launch_bounds__(kThreads)
 template <int SRC, int DST>
 cudaError_t run_pack(const dbuf_plan_t *p, const void *const *src, void *buf, cudaStream_t st) {
     const unsigned grid = unsigned(p->chunks.size());
-    pack_kernel<SRC, DST><<<grid, kThreads, 0, st>>>(p->dev.chunks, p->dev.tensors, src,
-                                                     static_cast<char *>(buf));
-    return cudaGetLastError();
+    return launch_pdl(pack_kernel<SRC, DST>, grid, kThreads, 0, st,
+                      static_cast<const Chunk *>(p->dev.chunks),
+                      static_cast<const TensorDesc *>(p->dev.tensors), src, static_cast<char *>(buf));
 }
 
 template <int SRC, int DST>
 cudaError_t run_unpack(const dbuf_plan_t *p, const void *buf, void *const *dst, cudaStream_t st) {
     const unsigned grid = unsigned(p->chunks.size());
-    unpack_kernel<SRC, DST><<<grid, kThreads, 0, st>>>(p->dev.chunks, p->dev.tensors,
-                                                       static_cast<const char *>(buf), dst);
-    return cudaGetLastError();
+    return launch_pdl(unpack_kernel<SRC, DST>, grid, kThreads, 0, st,
+                      static_cast<const Chunk *>(p->dev.chunks),
+                      static_cast<const TensorDesc *>(p->dev.tensors),
+                      static_cast<const char *>(buf), dst);
 }
 
 }  // namespace
@@ -153,13 +157,13 @@ int launch_sac(const dbuf_plan_t *p, void *grad, int gdt, float *acc, float scal
     if (p->chunks.empty()) return cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned grid = unsigned(p->chunks.size());
+    const Chunk *chunks = p->dev.chunks;
+    const TensorDesc *td = p->dev.tensors;
     if (gdt == DBUF_F32)
-        sac_kernel<DBUF_F32><<<grid, kThreads, 0, st>>>(p->dev.chunks, p->dev.tensors,
-                                                        static_cast<char *>(grad), acc, scale);
-    else
-        sac_kernel<DBUF_BF16><<<grid, kThreads, 0, st>>>(p->dev.chunks, p->dev.tensors,
-                                                         static_cast<char *>(grad), acc, scale);
-    return cudaGetLastError();
+        return launch_pdl(sac_kernel<DBUF_F32>, grid, kThreads, 0, st, chunks, td,
+                          static_cast<char *>(grad), acc, scale);
+    return launch_pdl(sac_kernel<DBUF_BF16>, grid, kThreads, 0, st, chunks, td,
+                      static_cast<char *>(grad), acc, scale);
 }
 
 }  // namespace dbuf

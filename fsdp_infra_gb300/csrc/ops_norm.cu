@@ -105,6 +105,7 @@ __global__ void __launch_bounds__(kThreads)
                 int32_t *__restrict__ nonfinite) {
     __shared__ double sh[kWarps];
     __shared__ int last;
+    pdl_enter();
     const Chunk c = chunks[blockIdx.x];
     const char *x = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<DT>();
     const int len = c.len;
@@ -228,15 +229,14 @@ int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_nor
     NormWorkspace w = carve(p, workspace);
     uint32_t nonempty = 0;
     for (const TensorDesc &d : p->tdesc) nonempty += d.chunk_end > d.chunk_begin ? 1u : 0u;
+    const Chunk *chunks = p->dev.chunks;
+    const TensorDesc *td = p->dev.tensors;
+    const char *b = static_cast<const char *>(buf);
     if (dt == DBUF_F32)
-        norm_kernel<DBUF_F32><<<nc, kThreads, 0, st>>>(p->dev.chunks, p->dev.tensors, p->n, nonempty,
-                                                        static_cast<const char *>(buf), w,
-                                                        tensor_norms, total_norm, nonfinite);
-    else
-        norm_kernel<DBUF_BF16><<<nc, kThreads, 0, st>>>(p->dev.chunks, p->dev.tensors, p->n,
-                                                         nonempty, static_cast<const char *>(buf),
-                                                         w, tensor_norms, total_norm, nonfinite);
-    return cudaGetLastError();
+        return launch_pdl(norm_kernel<DBUF_F32>, nc, kThreads, 0, st, chunks, td, p->n, nonempty, b,
+                          w, tensor_norms, total_norm, nonfinite);
+    return launch_pdl(norm_kernel<DBUF_BF16>, nc, kThreads, 0, st, chunks, td, p->n, nonempty, b, w,
+                      tensor_norms, total_norm, nonfinite);
 }
 
 }  // namespace dbuf

@@ -162,6 +162,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
                       const float *__restrict__ buf, uint8_t *__restrict__ codes,
                       float *__restrict__ scales) {
     __shared__ float sh_max[kTileWarps];
+    pdl_enter();
     const QItem it = items[blockIdx.x];
     const TensorDesc d = td[it.tensor];
     if (d.quant == DBUF_QUANT_E4M3) tile_body<DBUF_QUANT_E4M3>(it, d, buf, codes, scales, sh_max);
@@ -175,6 +176,7 @@ __global__ void __launch_bounds__(kTileThreads, 2)
                                 const TensorDesc *__restrict__ td, const float *__restrict__ buf,
                                 uint8_t *__restrict__ codes, float *__restrict__ scales) {
     __shared__ float sh_max[kTileWarps];
+    pdl_enter();
     const TileItem ti = items[blockIdx.x];
     const TensorDesc d = td[ti.tensor];
     const QItem it{int64_t(ti.bi) * d.nbc + ti.bj, ti.tensor, 1};
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(kThreads)
     quant_row_kernel(const RowItem *__restrict__ items, const TensorDesc *__restrict__ td,
                      const float *__restrict__ buf, uint8_t *__restrict__ codes,
                      float *__restrict__ scales) {
+    pdl_enter();
     const RowItem it = items[blockIdx.x];
     const TensorDesc d = td[it.tensor];
     if (d.quant == DBUF_QUANT_E4M3) row_body<DBUF_QUANT_E4M3>(it, d, buf, codes, scales);
@@ -382,6 +385,7 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     quant_pipe_kernel(const __grid_constant__ TmaMaps maps, const TileItem *__restrict__ items,
                       int nitems, const TensorDesc *__restrict__ td, uint8_t *__restrict__ codes,
                       float *__restrict__ scales, int32_t *__restrict__ status) {
+    pdl_enter();
     extern __shared__ unsigned char smem_raw[];
     // tensor copies land at 1024-byte-aligned buffers
     char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -558,28 +562,31 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
             const int n = int(i1 - i0);
             if (n == 0) continue;
             const int grid = n < p->dev.num_sms ? n : p->dev.num_sms;
-            quant_pipe_kernel<<<grid, kPipeThreads, kPipeSmemBytes, st>>>(
-                batches[b], p->dev.pipe_items + i0, n, p->dev.tensors, codes, scales,
-                p->dev.status);
-            cudaError_t e = cudaGetLastError();
+            const cudaError_t e = launch_pdl(
+                quant_pipe_kernel, grid, kPipeThreads, kPipeSmemBytes, st, batches[b],
+                static_cast<const TileItem *>(p->dev.pipe_items + i0), n,
+                static_cast<const TensorDesc *>(p->dev.tensors), codes, scales, p->dev.status);
             if (e != cudaSuccess) return e;
         }
     } else if (!p->pipe_items.empty()) {
-        quant_tile_pipe_list_kernel<<<unsigned(p->pipe_items.size()), kTileThreads, 0, st>>>(
-            p->dev.pipe_items, p->dev.tensors, buf, codes, scales);
-        cudaError_t e = cudaGetLastError();
+        const cudaError_t e = launch_pdl(
+            quant_tile_pipe_list_kernel, unsigned(p->pipe_items.size()), kTileThreads, 0, st,
+            static_cast<const TileItem *>(p->dev.pipe_items),
+            static_cast<const TensorDesc *>(p->dev.tensors), buf, codes, scales);
         if (e != cudaSuccess) return e;
     }
     if (!p->tile_items.empty()) {
-        quant_tile_kernel<<<unsigned(p->tile_items.size()), kTileThreads, 0, st>>>(
-            p->dev.tile_items, p->dev.tensors, buf, codes, scales);
-        cudaError_t e = cudaGetLastError();
+        const cudaError_t e = launch_pdl(
+            quant_tile_kernel, unsigned(p->tile_items.size()), kTileThreads, 0, st,
+            static_cast<const QItem *>(p->dev.tile_items),
+            static_cast<const TensorDesc *>(p->dev.tensors), buf, codes, scales);
         if (e != cudaSuccess) return e;
     }
     if (!p->row_items.empty()) {
-        quant_row_kernel<<<unsigned(p->row_items.size()), kThreads, 0, st>>>(
-            p->dev.row_items, p->dev.tensors, buf, codes, scales);
-        cudaError_t e = cudaGetLastError();
+        const cudaError_t e = launch_pdl(
+            quant_row_kernel, unsigned(p->row_items.size()), kThreads, 0, st,
+            static_cast<const RowItem *>(p->dev.row_items),
+            static_cast<const TensorDesc *>(p->dev.tensors), buf, codes, scales);
         if (e != cudaSuccess) return e;
     }
     return cudaSuccess;
