@@ -102,16 +102,34 @@ class DBuffer:
                 if x.device != self.device:
                     raise ValueError(f"tensor {t} is on {x.device}, expected {self.device}")
             ptrs = [k[0] for k in key] or [0]
-            tab = torch.tensor(ptrs, dtype=torch.int64, device=self.device)
+            tab = self._settled(torch.tensor(ptrs, dtype=torch.int64, device=self.device))
             self._ptr_tables[key] = tab
         return tab
 
+    def _settled(self, t: torch.Tensor) -> torch.Tensor:
+        """A cached device tensor just written on the current stream, made complete
+        before it is returned so that calls on any stream may use it (once per
+        cache entry; entries are made before any stream capture)."""
+        if not torch.cuda.is_current_stream_capturing():
+            torch.cuda.current_stream(self.device).synchronize()
+        return t
+
+    def workspace_bytes(self) -> int:
+        return _c.dbuf_workspace_bytes(self.handle, _c.DBUF_OP_NORM_NONFINITE)
+
+    def new_workspace(self) -> torch.Tensor:
+        """A norm workspace of its own, for a caller whose norm calls may overlap
+        those of other streams (zero-filled: the completion counters start at
+        zero and every call leaves them at zero again)."""
+        return self._settled(torch.zeros(max(self.workspace_bytes(), 1), dtype=torch.uint8,
+                                         device=self.device))
+
     def workspace(self) -> torch.Tensor:
-        nbytes = _c.dbuf_workspace_bytes(self.handle, _c.DBUF_OP_NORM_NONFINITE)
+        """The DBuffer's own norm workspace: calls that use it must not overlap on
+        the GPU (one stream at a time)."""
+        nbytes = self.workspace_bytes()
         if self._workspace is None or self._workspace.numel() < nbytes:
-            # zero-filled once: the norm's completion counters start at zero and
-            # every call leaves them at zero again
-            self._workspace = torch.zeros(nbytes, dtype=torch.uint8, device=self.device)
+            self._workspace = self.new_workspace()
         return self._workspace
 
     # -- group operators ---------------------------------------------------------
@@ -146,15 +164,18 @@ class DBuffer:
         _c.dbuf_scale_accum_zero(self.handle, grad.data_ptr(), dtype_code(grad.dtype),
                                  acc.data_ptr(), float(scale), self._stream(stream))
 
-    def norm_nonfinite(self, buf: torch.Tensor, out: Optional[Tuple] = None, stream=None):
-        """Returns device tensors (tensor_norms[n] f32, total_norm[1] f32, nonfinite[1] i32)."""
+    def norm_nonfinite(self, buf: torch.Tensor, out: Optional[Tuple] = None, stream=None,
+                       workspace: Optional[torch.Tensor] = None):
+        """Returns device tensors (tensor_norms[n] f32, total_norm[1] f32, nonfinite[1] i32).
+        `workspace` (from new_workspace) replaces the DBuffer's own for calls that may
+        overlap other streams' norm calls."""
         self._check_buf(buf)
         if out is None:
             out = (torch.empty(max(self.n, 1), dtype=torch.float32, device=self.device),
                    torch.empty(1, dtype=torch.float32, device=self.device),
                    torch.empty(1, dtype=torch.int32, device=self.device))
         norms, total, flag = out
-        ws = self.workspace()
+        ws = self.workspace() if workspace is None else workspace
         _c.dbuf_norm_nonfinite(self.handle, buf.data_ptr(), dtype_code(buf.dtype),
                                norms.data_ptr(), total.data_ptr(), flag.data_ptr(),
                                ws.data_ptr(), ws.numel(), self._stream(stream))
@@ -258,7 +279,7 @@ class DBuffer:
                 raise ValueError(f"{what} {t}: want a contiguous tensor of {numels[t]} "
                                  f"elements on {self.device}")
             ptrs.append(x.data_ptr())
-        tab = torch.tensor(ptrs or [0], dtype=torch.int64, device=self.device)
+        tab = self._settled(torch.tensor(ptrs or [0], dtype=torch.int64, device=self.device))
         self._ptr_tables[key] = tab
         return tab
 
