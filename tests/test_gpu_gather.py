@@ -35,29 +35,41 @@ def _host(t: torch.Tensor) -> np.ndarray:
     return a.view(torch.int16).numpy().view(np.uint16) if a.dtype == torch.bfloat16 else a.numpy()
 
 
+# A whole-matrix block of 50,000 elements forces S up to the block: with m=16
+# most shard slices are empty.
+SPECS_WHOLE = [TensorSpec("w", 200, 250, 200), TensorSpec("v", 100, 1, 1),
+               TensorSpec("e", 64, 64, 16), TensorSpec("z", 0, 8, 1)]
+
+
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
-@pytest.mark.parametrize("m,units,shift", [(4, None, 0), (7, None, 1), (5, [1, 3, 2, 1, 4], 0)])
-def test_gather_scatter_match_oracle(dbuf_lib, oracle_lib, dt, m, units, shift):
+@pytest.mark.parametrize("which,m,units,shift", [("mixed", 4, None, 0), ("mixed", 7, None, 1),
+                                                 ("mixed", 5, [1, 3, 2, 1, 4], 0),
+                                                 ("whole", 16, None, 0)])
+def test_gather_scatter_match_oracle(dbuf_lib, oracle_lib, dt, which, m, units, shift):
     from fsdp_infra_gb300 import DBuffer
+    SPECS_ = SPECS if which == "mixed" else SPECS_WHOLE
     rng = np.random.default_rng(m + shift)
-    op = oracle_lib.plan_specs(SPECS, m, units, 16)
-    db = DBuffer(SPECS, m, units, 16).upload()
+    op = oracle_lib.plan_specs(SPECS_, m, units, 16)
+    db = DBuffer(SPECS_, m, units, 16).upload()
+    if which == "whole":  # all tensor data in the first two slices, the other 14 only padding
+        assert db.S >= 50000
+        assert max(o + s.numel for o, s in zip(db.offsets, SPECS_)) <= 2 * db.S
     assert db.offsets == [int(x) for x in op.offsets]
     npdt = _np_dtype(dt)
     hs = [rng.integers(0, 2 ** 15, n).astype(npdt) for n in db.shard_sizes()]
     shards = [_to_dev(h, dt, shift) for h in hs]
     # gather every other tensor; the rest must stay as filled
-    hd = [None if t % 2 else np.full(s.numel, 3, npdt) for t, s in enumerate(SPECS)]
+    hd = [None if t % 2 else np.full(s.numel, 3, npdt) for t, s in enumerate(SPECS_)]
     dd = [None if x is None else _to_dev(x, dt, shift) for x in hd]
     db.gather(shards, dd)
     oracle_lib.gather(op, hs, hd)
     torch.cuda.synchronize()
-    for t in range(len(SPECS)):
+    for t in range(len(SPECS_)):
         if hd[t] is not None:
             assert np.array_equal(_host(dd[t]), hd[t]), f"gather t{t}"
     # scatter new matrices for the odd tensors
     hsrc = [None if t % 2 == 0 else rng.integers(0, 2 ** 15, s.numel).astype(npdt)
-            for t, s in enumerate(SPECS)]
+            for t, s in enumerate(SPECS_)]
     dsrc = [None if x is None else _to_dev(x, dt, shift) for x in hsrc]
     db.scatter(dsrc, shards)
     oracle_lib.scatter(op, hsrc, hs)
