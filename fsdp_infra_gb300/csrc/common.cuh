@@ -151,6 +151,23 @@ __device__ __forceinline__ bool aligned16(const void *a, const void *b) {
     return ((reinterpret_cast<uintptr_t>(a) | reinterpret_cast<uintptr_t>(b)) & 15u) == 0;
 }
 
+// The elementwise kernels run kChunkSplit CTAs per chunk, each over one part of
+// kSubElems elements (a multiple of 8 elements, so a part starts 16-byte
+// aligned whenever its chunk does): smaller CTAs shorten the drain of a launch
+// without changing the chunk table the norm's partials are kept per.
+constexpr int kChunkSplit = 2;
+constexpr int kSubElems = int(kChunkElems / kChunkSplit);
+static_assert(kSubElems % kVec == 0, "parts keep vector alignment");
+
+// This CTA's part of its chunk (len 0 when the chunk is shorter than the part's start).
+__device__ __forceinline__ Chunk sub_chunk(const Chunk *__restrict__ chunks) {
+    Chunk c = chunks[blockIdx.x / kChunkSplit];
+    const int start = int(blockIdx.x % kChunkSplit) * kSubElems;
+    c.off += start;
+    c.len = max(0, min(c.len - start, kSubElems));
+    return c;
+}
+
 // Programmatic dependent launch.  A kernel launched with launch_pdl may be
 // scheduled while the previous kernel of its stream is still running; it must
 // call pdl_enter before its first access to global memory: the wait returns once

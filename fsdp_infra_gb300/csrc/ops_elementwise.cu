@@ -9,9 +9,9 @@
 // mixed precision (one cast per flat parameter), gradient accumulation.
 //
 // Work split: the plan's chunk table cuts every tensor into chunks of at most
-// kChunkElems elements; one CTA handles one chunk with 16-byte vector loads and
-// stores (8 elements per thread per unit, kUnroll units in flight per thread),
-// and a scalar tail.  Padding between tensors is never touched.
+// kChunkElems elements; kChunkSplit CTAs share a chunk, each handling its part
+// with 16-byte vector loads and stores (8 elements per thread per unit, kUnroll
+// units in flight per thread), and a scalar tail.  Padding between tensors is never touched.
 #include "common.cuh"
 
 namespace dbuf {
@@ -44,7 +44,7 @@ __global__ void __launch_bounds__(kThreads)
     pack_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                 const void *const *__restrict__ src, char *__restrict__ buf) {
     pdl_enter();
-    const Chunk c = chunks[blockIdx.x];
+    const Chunk c = sub_chunk(chunks);
     const char *s = static_cast<const char *>(src[c.tensor]) + c.off * elem_bytes<SRC>();
     char *d = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<DST>();
     copy_cast_range<SRC, DST>(s, d, c.len);
@@ -55,7 +55,7 @@ __global__ void __launch_bounds__(kThreads)
     unpack_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                   const char *__restrict__ buf, void *const *__restrict__ dst) {
     pdl_enter();
-    const Chunk c = chunks[blockIdx.x];
+    const Chunk c = sub_chunk(chunks);
     const char *s = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<SRC>();
     char *d = static_cast<char *>(dst[c.tensor]) + c.off * elem_bytes<DST>();
     copy_cast_range<SRC, DST>(s, d, c.len);
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kThreads)
     sac_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                char *__restrict__ grad, float *__restrict__ acc, float scale) {
     pdl_enter();
-    const Chunk c = chunks[blockIdx.x];
+    const Chunk c = sub_chunk(chunks);
     const int64_t base = td[c.tensor].buf_off + c.off;
     char *g = grad + base * elem_bytes<GDT>();
     char *a = reinterpret_cast<char *>(acc + base);
@@ -116,7 +116,7 @@ __global__ void __launch_bounds__(kThreads)
 
 template <int SRC, int DST>
 cudaError_t run_pack(const dbuf_plan_t *p, const void *const *src, void *buf, cudaStream_t st) {
-    const unsigned grid = unsigned(p->chunks.size());
+    const unsigned grid = unsigned(p->chunks.size()) * kChunkSplit;
     return launch_pdl(pack_kernel<SRC, DST>, grid, kThreads, 0, st,
                       static_cast<const Chunk *>(p->dev.chunks),
                       static_cast<const TensorDesc *>(p->dev.tensors), src, static_cast<char *>(buf));
@@ -124,7 +124,7 @@ cudaError_t run_pack(const dbuf_plan_t *p, const void *const *src, void *buf, cu
 
 template <int SRC, int DST>
 cudaError_t run_unpack(const dbuf_plan_t *p, const void *buf, void *const *dst, cudaStream_t st) {
-    const unsigned grid = unsigned(p->chunks.size());
+    const unsigned grid = unsigned(p->chunks.size()) * kChunkSplit;
     return launch_pdl(unpack_kernel<SRC, DST>, grid, kThreads, 0, st,
                       static_cast<const Chunk *>(p->dev.chunks),
                       static_cast<const TensorDesc *>(p->dev.tensors),
@@ -156,7 +156,7 @@ int launch_unpack(const dbuf_plan_t *p, const void *buf, int bdt, void *const *d
 int launch_sac(const dbuf_plan_t *p, void *grad, int gdt, float *acc, float scale, void *stream) {
     if (p->chunks.empty()) return cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const unsigned grid = unsigned(p->chunks.size());
+    const unsigned grid = unsigned(p->chunks.size()) * kChunkSplit;
     const Chunk *chunks = p->dev.chunks;
     const TensorDesc *td = p->dev.tensors;
     if (gdt == DBUF_F32)

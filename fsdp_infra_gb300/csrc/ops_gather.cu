@@ -53,7 +53,12 @@ template <bool GATHER>
 __global__ void __launch_bounds__(kThreads)
     piece_copy_kernel(const Piece *__restrict__ pieces, void *const *__restrict__ shards,
                       void *const *__restrict__ tensors, int es) {
-    const Piece pc = pieces[blockIdx.x];
+    // kChunkSplit CTAs per piece, as the elementwise kernels split their chunks
+    Piece pc = pieces[blockIdx.x / kChunkSplit];
+    const int start = int(blockIdx.x % kChunkSplit) * kSubElems;
+    pc.off += start;
+    pc.shard_off += start;
+    pc.len = max(0, min(pc.len - start, kSubElems));
     char *tp = static_cast<char *>(tensors[pc.tensor]);
     if (!tp) return;
     char *sp = static_cast<char *>(shards[pc.shard]);
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(kThreads)
 int launch_gather(const dbuf_plan_t *p, void *const *shards, int dt, void *const *dst,
                   void *stream) {
     if (p->pieces.empty()) return cudaSuccess;
-    piece_copy_kernel<true><<<unsigned(p->pieces.size()), kThreads, 0,
+    piece_copy_kernel<true><<<unsigned(p->pieces.size()) * kChunkSplit, kThreads, 0,
                               static_cast<cudaStream_t>(stream)>>>(
         p->dev.pieces, shards, dst, dt == DBUF_F32 ? 4 : 2);
     return cudaGetLastError();
@@ -79,7 +84,7 @@ int launch_gather(const dbuf_plan_t *p, void *const *shards, int dt, void *const
 int launch_scatter(const dbuf_plan_t *p, const void *const *src, int dt, void *const *shards,
                    void *stream) {
     if (p->pieces.empty()) return cudaSuccess;
-    piece_copy_kernel<false><<<unsigned(p->pieces.size()), kThreads, 0,
+    piece_copy_kernel<false><<<unsigned(p->pieces.size()) * kChunkSplit, kThreads, 0,
                                static_cast<cudaStream_t>(stream)>>>(
         p->dev.pieces, shards, const_cast<void *const *>(src), dt == DBUF_F32 ? 4 : 2);
     return cudaGetLastError();

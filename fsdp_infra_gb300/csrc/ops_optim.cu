@@ -249,7 +249,7 @@ __global__ void __launch_bounds__(kThreads)
                  const int32_t *__restrict__ nonfinite) {
     if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
     const AdamScalars s = adam_scalars(hp, total_norm);
-    const Chunk c = chunks[blockIdx.x];
+    const Chunk c = sub_chunk(chunks);
     const int64_t base = td[c.tensor].buf_off + c.off;
     adamw_range(s, params + base, grads + base, exp_avg + base, exp_avg_sq + base, c.len);
 }
@@ -1092,7 +1092,7 @@ int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float 
                  const int32_t *nonfinite, void *stream) {
     if (p->chunks.empty()) return cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
-    adamw_kernel<<<unsigned(p->chunks.size()), kThreads, 0, st>>>(
+    adamw_kernel<<<unsigned(p->chunks.size()) * kChunkSplit, kThreads, 0, st>>>(
         p->dev.chunks, p->dev.tensors, params, grads, exp_avg, exp_avg_sq, hp, total_norm,
         nonfinite);
     return cudaGetLastError();
