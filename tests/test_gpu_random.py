@@ -1,0 +1,69 @@
+"""Seeded random groups against the oracle.
+
+Each case draws a tensor group (vectors and matrices of random sizes, empty
+tensors, block shapes 128x128, 64x128, 32x32, 16x16, 1x128, 1x64 and an odd 5x4
+with ragged edges, E4M3 and INT8, unquantised matrices at 1-, 4- and
+whole-tensor row granularity), a shard count m in 1..9, even or uneven
+local_units, alignment 1 or 16, and fp32 or bf16 gradients; every operator runs
+on the GPU and is compared with the oracle on whole buffers (two accumulation
+steps).  The 8-bit AdamW cases draw groups the same way and take two steps
+against the oracle.  The cases are reproducible from their seed.
+"""
+import numpy as np
+import pytest
+import torch
+
+from workloads.configs import TensorSpec
+
+from test_gpu_optim8 import Case
+from test_gpu_parity import full_group_parity
+
+pytestmark = pytest.mark.gpu
+
+BLOCKS = [(128, 128), (64, 128), (32, 32), (16, 16), (1, 128), (1, 64), (5, 4)]
+
+
+def random_group(rng):
+    specs = []
+    for t in range(int(rng.integers(1, 13))):
+        kind = rng.random()
+        if kind < 0.25:
+            specs.append(TensorSpec(f"v{t}", int(rng.integers(0, 3000)), 1, 1))
+        elif kind < 0.45:
+            rows, cols = int(rng.integers(1, 300)), int(rng.integers(1, 200))
+            gran = [1, 4, rows][int(rng.integers(0, 3))]
+            specs.append(TensorSpec(f"m{t}", rows, cols, gran))
+        else:
+            qb = BLOCKS[int(rng.integers(0, len(BLOCKS)))]
+            rows = int(rng.integers(0, 3 * qb[0] + 40))
+            cols = int(rng.integers(1, 3 * qb[1] + 20))
+            quant = "e4m3" if rng.random() < 0.5 else "int8"
+            specs.append(TensorSpec(f"q{t}", rows, cols, qb[0], qblock=qb, quant=quant))
+    m = int(rng.integers(1, 10))
+    units = [int(u) for u in rng.integers(1, 5, m)] if rng.random() < 0.3 else None
+    align = 16 if rng.random() < 0.7 else 1
+    return specs, m, units, align
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_group_all_operators(dbuf_lib, oracle_lib, seed):
+    rng = np.random.default_rng(1000 + seed)
+    specs, m, units, align = random_group(rng)
+    gdt = torch.bfloat16 if rng.random() < 0.3 else torch.float32
+    gen = torch.Generator().manual_seed(seed)
+    params = [torch.randn(s.rows, s.cols, generator=gen) * 0.02 for s in specs]
+    full_group_parity(oracle_lib, specs, m, units, align,
+                      param_fn=lambda t: params[t],
+                      grad_fn=lambda t, step: (torch.randn(specs[t].rows, specs[t].cols,
+                                                           generator=gen) * 1e-3).to(gdt),
+                      grad_dtype=gdt, scale=1.0 / max(m, 1), accum_steps=2)
+
+
+@pytest.mark.parametrize("seed", range(10))
+def test_random_group_adamw8(dbuf_lib, oracle_lib, seed):
+    rng = np.random.default_rng(2000 + seed)
+    specs, m, units, align = random_group(rng)
+    c = Case(oracle_lib, specs, m, units=units, align=align, seed=seed,
+             shift=1 if rng.random() < 0.2 else 0)
+    c.step(1, clip=True)
+    c.step(2)
