@@ -538,6 +538,21 @@ bool encode_maps(const dbuf_plan_t *p, const float *buf, TmaMaps *maps, size_t b
 
 }  // namespace
 
+// Persistent grid of the pipelined tile kernel for n tiles on `sms` SMs.  CTA b
+// takes tiles b, b + G, ... and its two groups alternate, so a launch lasts as
+// many tile rounds as its busiest group has tiles: ceil(ceil(n / G) / 2).  With
+// G = sms that is the fewest rounds; from two rounds per group on, the grid is
+// then cut to the fewest CTAs that still finish in those rounds (at least 90%
+// of the SMs): the same bytes in the same rounds on fewer, fuller groups.
+static int pipe_grid(int n, int sms) {
+    if (n < 4 * sms) return n < sms ? n : sms;
+    const int rounds = ((n + sms - 1) / sms + 1) / 2;
+    const int per_cta = 2 * rounds;
+    const int g = (n + per_cta - 1) / per_cta;
+    const int lo = (9 * sms + 9) / 10;
+    return g < lo ? lo : g;
+}
+
 int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *scales,
                  void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -561,7 +576,7 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
             const size_t i1 = p->pipe_item_start[std::min(nslot, b0 + kPipeMaxTensors)];
             const int n = int(i1 - i0);
             if (n == 0) continue;
-            const int grid = n < p->dev.num_sms ? n : p->dev.num_sms;
+            const int grid = pipe_grid(n, p->dev.num_sms);
             const cudaError_t e = launch_pdl(
                 quant_pipe_kernel, grid, kPipeThreads, kPipeSmemBytes, st, batches[b],
                 static_cast<const TileItem *>(p->dev.pipe_items + i0), n,
