@@ -466,16 +466,25 @@ def _traffic_for(kernel_key):
     return None
 
 
-def op_alone_ms(stack, op, eager, passes=3):
+def op_alone_ms(stack, op, eager, passes=3, min_launches=32):
     """Milliseconds of one pass of `op` over every DBuffer: the launches back to
     back (captured as one graph unless eager), one untimed pass, then `passes`
-    timed ones between two events.  Each pass moves far more than L2 holds."""
+    timed ones between two events.  Each pass moves far more than L2 holds.  A
+    workload of few DBuffers repeats its pass inside the graph until it holds at
+    least `min_launches` DBuffer launches, so that the graph's own launch cost is
+    not charged to one or two kernels."""
+    reps = max(1, -(-min_launches // max(1, len(stack.dbufs))))
+
+    def one():
+        for _ in range(reps):
+            stack.run_op(op)
+
     graph = None
     if not eager:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
-            stack.run_op(op)
-    run = graph.replay if graph is not None else (lambda: stack.run_op(op))
+            one()
+    run = graph.replay if graph is not None else one
     run()
     torch.cuda.synchronize()
     s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -484,7 +493,7 @@ def op_alone_ms(stack, op, eager, passes=3):
         run()
     e.record()
     torch.cuda.synchronize()
-    return s.elapsed_time(e) / passes
+    return s.elapsed_time(e) / (passes * reps)
 
 
 def run_ours(args):
@@ -631,6 +640,8 @@ def run_ours(args):
                 "ops_note": ("per operator, outside the timed region: its launches over every "
                              "DBuffer back to back, timed over 3 passes" +
                              ("" if args.eager else " of one graph") +
+                             (f" (each pass repeated {-(-32 // len(stack.dbufs))}x, "
+                              "at least 32 launches)" if len(stack.dbufs) < 32 else "") +
                              "; evented_*: one step with events around every launch"),
                 "clocks": clock_info, "ops": ops}
         print(json.dumps(line), flush=True)
