@@ -440,10 +440,10 @@ def _config_dict(stack, key):
     return d
 
 
-def _traffic_for(kernel_key):
-    """dram bytes per launch recorded from an ncu capture (profiles/dram_traffic.txt),
-    or None if any source file of that kernel changed since (the record carries
-    the files' sha256 prefixes)."""
+def _traffic_for(kernel_key, workload_key):
+    """dram bytes per launch recorded from an ncu capture (profiles/dram_traffic.txt)
+    of this workload, or None if there is none or any source file of that kernel
+    changed since (the record carries the files' sha256 prefixes)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
@@ -454,6 +454,8 @@ def _traffic_for(kernel_key):
                 continue
             kv = dict(x.split("=", 1) for x in line.split())
             if kv.get("op") != kernel_key:
+                continue
+            if kv.get("workload", "").split("-")[0] != workload_key:
                 continue
             for name, sha in zip(kv["files"].split(","), kv["sha"].split(",")):
                 try:
@@ -603,7 +605,7 @@ def run_ours(args):
                 "peak_kind": peak_kind, "unit": "GB/s", "frac": round(achieved / peak, 4),
                 "frac_of_nominal_8tbs": round(achieved / NOMINAL_HBM_GBS, 4),
                 "bytes_per_launch": layer_bytes,
-                "traffic": _traffic_for(dom)}
+                "traffic": _traffic_for(dom, stack.w.key)}
 
     # ---- the next row: fused AdamW step over every DBuffer (separate timing)
     adamw = None if args.no_adamw else run_adamw(stack, args, world, peak, barrier)
@@ -705,7 +707,7 @@ def run_adamw(stack, args, world, peak, barrier):
             "params_per_s": round(world * stack.elements / (ms / 1e3), 1),
             "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 28,
             "launches_per_step": len(stack.dbufs),
-            "traffic_layer_launch": _traffic_for("adamw"),
+            "traffic_layer_launch": _traffic_for("adamw", stack.w.key),
             "algorithmic_layer_launch": 28 * stack.w.groups[0].numel}
 
 
@@ -787,7 +789,7 @@ def run_adamw8(stack, args, world, peak, barrier):
             "frac_of_peak": round(gbs / world / peak, 4),
             "bytes_per_step": nbytes, "flat_elements_per_step": elems,
             "launches_per_step": sum(kinds[gi]["launches"] for gi in order),
-            "traffic_layer_launch": _traffic_for("adamw8"),
+            "traffic_layer_launch": _traffic_for("adamw8", stack.w.key),
             "algorithmic_layer_launch": kinds[0]["bytes"]}
 
 
@@ -842,8 +844,8 @@ def run_gather(stack, args, world, peak, barrier):
             "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),
             "frac_of_peak": round(gbs / world / peak, 4), "bytes_per_elem": 16,
             "launches_per_step": 2 * len(stack.dbufs),
-            "traffic_layer_launch": {"gather": _traffic_for("gather"),
-                                     "scatter": _traffic_for("scatter")},
+            "traffic_layer_launch": {"gather": _traffic_for("gather", stack.w.key),
+                                     "scatter": _traffic_for("scatter", stack.w.key)},
             "algorithmic_layer_launch": 8 * stack.w.groups[0].numel}
 
 
