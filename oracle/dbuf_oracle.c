@@ -280,6 +280,20 @@ static void store_elem(void *p, int32_t dtype, int64_t i, float v)
     else ((float *)p)[i] = v;
 }
 
+/* One element from src[i] to dst[j]: a copy of its bytes when both sides have
+ * the same type (a copy-in or copy-out is a copy, so every bit pattern, NaN
+ * payloads included, arrives unchanged), else the cast through fp32. */
+static void move_elem(const void *src, int32_t src_dtype, int64_t i,
+                      void *dst, int32_t dst_dtype, int64_t j)
+{
+    if (src_dtype == dst_dtype) {
+        size_t w = src_dtype == ORC_BF16 ? 2 : 4;
+        memcpy((char *)dst + (size_t)j * w, (const char *)src + (size_t)i * w, w);
+        return;
+    }
+    store_elem(dst, dst_dtype, j, load_elem(src, src_dtype, i));
+}
+
 /* pack (copy-in), with the mixed-precision cast fused: buf[l_t + i] =
  * cast(src_t[i]) for every tensor t [FSDP-1, §5 DBuffer group-level operators
  * and zero-copy access; FSDP-2, native mixed precision].  Padding between
@@ -289,7 +303,7 @@ void orc_pack(int32_t n, const int64_t *offsets, const int64_t *numel,
 {
     for (int32_t t = 0; t < n; ++t)
         for (int64_t i = 0; i < numel[t]; ++i)
-            store_elem(buf, buf_dtype, offsets[t] + i, load_elem(src[t], src_dtype, i));
+            move_elem(src[t], src_dtype, i, buf, buf_dtype, offsets[t] + i);
 }
 
 /* unpack (copy-out / reconstruct a tensor from the flat buffer):
@@ -299,7 +313,7 @@ void orc_unpack(int32_t n, const int64_t *offsets, const int64_t *numel,
 {
     for (int32_t t = 0; t < n; ++t)
         for (int64_t i = 0; i < numel[t]; ++i)
-            store_elem(dst[t], dst_dtype, i, load_elem(buf, buf_dtype, offsets[t] + i));
+            move_elem(buf, buf_dtype, offsets[t] + i, dst[t], dst_dtype, i);
 }
 
 /* Gradient scale, accumulate and zero over the tensor ranges, in buffer order:

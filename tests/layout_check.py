@@ -139,3 +139,45 @@ def naive_concat(specs, m, align=1):
     S = -(-e // m)
     S = (S + align - 1) // align * align
     return S, offs, [k * S for k in range(m + 1)]
+
+
+def literal_greedy(specs, U, m, units, align, window=512) -> Optional[List[int]]:
+    """Greedy-leftmost offsets at unit size U by a literal scan, or None.
+
+    Each tensor starts at the smallest aligned p >= the previous tensor's end
+    such that the tensor ends inside the buffer (iv) and every boundary strictly
+    inside [p, p + n) lies a multiple of g_t from p (iii).  The candidate starts
+    are examined in increasing order, a window of them at a time (vectorised);
+    nothing is skipped by reasoning about the constraint's structure.
+    """
+    B = np.asarray(boundaries(U, m, units), dtype=np.int64)
+    top = int(B[-1])
+    inner = B[1:-1]
+    offs: List[int] = []
+    e = 0
+    for s in specs:
+        n = s.rows * s.cols
+        g = max(1, unit_of(s.rows, s.cols, s.gran_rows))
+        p0 = -(-e // align) * align
+        found = None
+        w = window
+        while p0 + n <= top:
+            cand = p0 + align * np.arange(w, dtype=np.int64)
+            cand = cand[cand + n <= top]
+            if cand.size == 0:
+                break
+            ok = np.ones(cand.size, dtype=bool)
+            near = inner[(inner > cand[0]) & (inner < cand[-1] + n)]
+            for b in near:
+                ok &= ~((cand < b) & (b < cand + n) & ((b - cand) % g != 0))
+            hit = np.flatnonzero(ok)
+            if hit.size:
+                found = int(cand[hit[0]])
+                break
+            p0 = int(cand[-1]) + align
+            w = min(2 * w, 1 << 21)
+        if found is None:
+            return None
+        offs.append(found)
+        e = found + n
+    return offs
