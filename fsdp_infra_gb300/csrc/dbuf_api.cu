@@ -2,6 +2,7 @@
 // descriptor-table upload, and dispatch to the group-operator launchers.
 #include <cuda_runtime.h>
 
+#include <cmath>
 #include <cstring>
 
 #include "dbuf_internal.h"
@@ -202,15 +203,26 @@ extern "C" int dbuf_device_status(const dbuf_plan_t *p, int32_t *status, void *s
     return DBUF_OK;
 }
 
+bool dbuf::adam_params(const dbuf_adamw_hparams &hp, AdamParams *out) {
+    if (hp.step < 1) return false;
+    const double t = double(hp.step);
+    const float bc1 = float(1.0 - std::pow(double(hp.beta1), t));
+    const float bc2 = float(1.0 - std::pow(double(hp.beta2), t));
+    if (!(bc1 > 0.0f) || !(bc2 > 0.0f) || !std::isfinite(bc1) || !std::isfinite(bc2))
+        return false;
+    *out = AdamParams{hp.lr, hp.beta1, hp.beta2, hp.eps, hp.weight_decay, bc1, bc2, hp.max_norm};
+    return true;
+}
+
 extern "C" int dbuf_adamw_step(const dbuf_plan_t *p, float *params, const float *grads,
                                float *exp_avg, float *exp_avg_sq, const dbuf_adamw_hparams *hp,
                                const float *total_norm, const int32_t *nonfinite, void *stream) {
+    dbuf::AdamParams ap;
+    if (!p || !hp || !dbuf::adam_params(*hp, &ap)) return DBUF_EINVAL;
     int rc = check_plan(p);
     if (rc) return rc;
-    if (!hp || !(hp->bias_correction1 > 0.0f) || !(hp->bias_correction2 > 0.0f))
-        return DBUF_EINVAL;
     if (p->n > 0 && (!params || !grads || !exp_avg || !exp_avg_sq)) return DBUF_EINVAL;
-    return finish(dbuf::launch_adamw(p, params, grads, exp_avg, exp_avg_sq, *hp, total_norm,
+    return finish(dbuf::launch_adamw(p, params, grads, exp_avg, exp_avg_sq, ap, total_norm,
                                      nonfinite, stream));
 }
 
@@ -220,10 +232,10 @@ extern "C" int dbuf_adamw8_step(const dbuf_plan_t *p, float *params, const float
                                 float *exp_avg_fp32, float *exp_avg_sq_fp32,
                                 const dbuf_adamw_hparams *hp, const float *total_norm,
                                 const int32_t *nonfinite, void *stream) {
+    dbuf::AdamParams ap;
+    if (!p || !hp || !dbuf::adam_params(*hp, &ap)) return DBUF_EINVAL;
     int rc = check_plan(p);
     if (rc) return rc;
-    if (!hp || !(hp->bias_correction1 > 0.0f) || !(hp->bias_correction2 > 0.0f))
-        return DBUF_EINVAL;
     if (p->n > 0 && (!params || !grads)) return DBUF_EINVAL;
     if (p->n_scales > 0 &&
         (!exp_avg_codes || !exp_avg_sq_codes || !exp_avg_scales || !exp_avg_sq_scales))
@@ -231,7 +243,7 @@ extern "C" int dbuf_adamw8_step(const dbuf_plan_t *p, float *params, const float
     if (p->n_state > 0 && (!exp_avg_fp32 || !exp_avg_sq_fp32)) return DBUF_EINVAL;
     return finish(dbuf::launch_adamw8(p, params, grads, exp_avg_codes, exp_avg_sq_codes,
                                       exp_avg_scales, exp_avg_sq_scales, exp_avg_fp32,
-                                      exp_avg_sq_fp32, *hp, total_norm, nonfinite, stream));
+                                      exp_avg_sq_fp32, ap, total_norm, nonfinite, stream));
 }
 
 extern "C" int dbuf_gather(const dbuf_plan_t *p, void *const *shards, int32_t dtype,

@@ -126,6 +126,23 @@ constexpr int kPipeMaxRows = 128;
 constexpr int kPipeMaxCols = 128;
 constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch; more tensors take more launches
 
+// The scalars of one AdamW step as the kernels take them: the caller's
+// hyperparameters with the bias corrections formed (see bias_corrections).
+struct AdamParams {
+    float lr;
+    float beta1;
+    float beta2;
+    float eps;
+    float weight_decay;
+    float bias_correction1;  // 1 - beta1^t
+    float bias_correction2;  // 1 - beta2^t
+    float max_norm;
+};
+
+// AdamParams from the ABI struct: bc = (float)(1 - pow((double)beta, (double)t)).
+// Returns false for t < 1 or a correction that is not a positive finite float.
+bool adam_params(const dbuf_adamw_hparams &hp, AdamParams *out);
+
 struct DeviceTables {
     TensorDesc *tensors = nullptr;
     Chunk *chunks = nullptr;
@@ -157,12 +174,12 @@ int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *
                  void *stream);
 
 int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
-                 float *exp_avg_sq, const dbuf_adamw_hparams &hp, const float *total_norm,
+                 float *exp_avg_sq, const AdamParams &hp, const float *total_norm,
                  const int32_t *nonfinite, void *stream);
 
 int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8_t *m_codes,
                   uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
-                  const dbuf_adamw_hparams &hp, const float *total_norm, const int32_t *nonfinite,
+                  const AdamParams &hp, const float *total_norm, const int32_t *nonfinite,
                   void *stream);
 
 int launch_gather(const dbuf_plan_t *p, void *const *shards, int dt, void *const *dst,
@@ -171,6 +188,9 @@ int launch_scatter(const dbuf_plan_t *p, const void *const *src, int dt, void *c
                    void *stream);
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p);
+// Where the norm's completion tickets (n + 1 uint32) sit in its workspace.
+size_t norm_ticket_offset(const dbuf_plan_t *p);
+size_t norm_ticket_bytes(const dbuf_plan_t *p);
 
 // One-time per-device set-up of the quantisation kernels (shared memory
 // limits); called from dbuf_plan_upload.  Returns a cudaError_t value.

@@ -12,16 +12,18 @@
 // every device loading the library holds until the process exits.  Host code
 // cannot use the array's name as a device address, so the first call on each
 // device (with that device current) asks the runtime for the array's device
-// address once and caches it; later calls reuse it.  The call then runs the
-// same two kernels as dbuf_norm_nonfinite with that address as the workspace.
-// The only scratch words that must start at zero are the completion tickets:
-// the array is zero when the library is loaded, and every call returns each
-// ticket it used to zero before it finishes, so each call finds them cleared;
-// every partial sum, flag and per-tensor sum a call reads is written earlier in
-// the same call, so nothing else depends on what a previous call left behind.
+// address once and caches it; later calls reuse it.  A cudaDeviceReset after
+// that first call is not supported: the cached address would be stale.
+// Each call first clears the completion tickets in the array (a memset on the
+// caller's stream; the only scratch words that must start at zero), then runs
+// the same norm kernel as dbuf_norm_nonfinite with the array as its workspace.
+// Every partial sum, flag and per-tensor sum a call reads is written earlier in
+// the same call, so a call never depends on what an earlier call left behind,
+// even one that overlapped another and raced on the tickets.
 // All calls share the one array, so calls that overlap on the GPU (different
-// streams, or several host threads) race on it and must be serialised by the
-// caller.  No cudaMalloc, cudaFree or other allocating routine is called.
+// streams, or several host threads) race on it and their results are not
+// valid; the caller must serialise them.  No cudaMalloc, cudaFree or other
+// allocating routine is called.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -75,6 +77,12 @@ extern "C" int dbuf_norm_nonfinite_noalloc(const dbuf_plan_t *p, const void *buf
     int rc = scratch_address(dev, &scratch);
     if (rc != int(cudaSuccess)) {
         dbuf::record_cuda_error(rc);
+        return DBUF_ECUDA;
+    }
+    e = cudaMemsetAsync(static_cast<char *>(scratch) + dbuf::norm_ticket_offset(p), 0,
+                        dbuf::norm_ticket_bytes(p), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) {
+        dbuf::record_cuda_error(int(e));
         return DBUF_ECUDA;
     }
     rc = dbuf::launch_norm(p, buf, dtype, tensor_norms, total_norm, nonfinite, scratch, stream);

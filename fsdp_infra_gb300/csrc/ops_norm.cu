@@ -218,6 +218,14 @@ size_t norm_workspace_bytes(const dbuf_plan_t *p) {
            align256(sizeof(uint32_t) * (n + 1));
 }
 
+size_t norm_ticket_offset(const dbuf_plan_t *p) {
+    const size_t nc = p->chunks.size(), n = size_t(p->n);
+    return align256(sizeof(double) * nc) + align256(sizeof(int32_t) * nc) +
+           align256(sizeof(double) * n) + align256(sizeof(int32_t) * n);
+}
+
+size_t norm_ticket_bytes(const dbuf_plan_t *p) { return sizeof(uint32_t) * (size_t(p->n) + 1); }
+
 int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_norms,
                 float *total_norm, int32_t *nonfinite, void *workspace, void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);

@@ -45,7 +45,7 @@ struct AdamScalars {
 };
 
 // The clipping coefficient min(1, max_norm / (total_norm + 1e-6)), 1 without clipping.
-__device__ __forceinline__ float clip_coef(const dbuf_adamw_hparams &hp, const float *total_norm) {
+__device__ __forceinline__ float clip_coef(const AdamParams &hp, const float *total_norm) {
     if (hp.max_norm > 0.0f && total_norm) {
         const float c = __fdiv_rn(hp.max_norm, __fadd_rn(*total_norm, 1e-6f));
         return c < 1.0f ? c : 1.0f;
@@ -53,7 +53,7 @@ __device__ __forceinline__ float clip_coef(const dbuf_adamw_hparams &hp, const f
     return 1.0f;
 }
 
-__device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp,
+__device__ __forceinline__ AdamScalars adam_scalars(const AdamParams &hp,
                                                     const float *total_norm) {
     AdamScalars s;
     s.coef = clip_coef(hp, total_norm);
@@ -76,7 +76,7 @@ __device__ __forceinline__ AdamScalars adam_scalars(const dbuf_adamw_hparams &hp
 // operation is one IEEE single-precision operation rounded to nearest, as on
 // the device; a volatile result keeps every product and quotient rounded on
 // its own (no contraction into a fused multiply-add).
-AdamScalars host_scalars(const dbuf_adamw_hparams &hp) {
+AdamScalars host_scalars(const AdamParams &hp) {
     AdamScalars s;
     volatile float t;
     s.coef = 1.0f;
@@ -245,7 +245,7 @@ __global__ void __launch_bounds__(kThreads)
     adamw_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
                  float *__restrict__ params, const float *__restrict__ grads,
                  float *__restrict__ exp_avg, float *__restrict__ exp_avg_sq,
-                 const dbuf_adamw_hparams hp, const float *__restrict__ total_norm,
+                 const AdamParams hp, const float *__restrict__ total_norm,
                  const int32_t *__restrict__ nonfinite) {
     if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
     const AdamScalars s = adam_scalars(hp, total_norm);
@@ -725,7 +725,7 @@ __global__ void __launch_bounds__(kThreads, 4)
                   const TensorDesc *__restrict__ td, float *__restrict__ params,
                   const float *__restrict__ grads, uint8_t *__restrict__ mc,
                   uint8_t *__restrict__ vc, float *__restrict__ ms, float *__restrict__ vs,
-                  float *__restrict__ m32, float *__restrict__ v32, const dbuf_adamw_hparams hp,
+                  float *__restrict__ m32, float *__restrict__ v32, const AdamParams hp,
                   const float *__restrict__ total_norm, const int32_t *__restrict__ nonfinite) {
     __shared__ float2 red[2][kThreads / 32];
     if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
@@ -841,7 +841,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     adamw8_pipe_kernel(const __grid_constant__ P8Maps maps, const P8Item *__restrict__ items,
                        int nitems, const TensorDesc *__restrict__ td, float *__restrict__ params,
                        uint8_t *__restrict__ mc, uint8_t *__restrict__ vc, float *__restrict__ ms,
-                       float *__restrict__ vs, const dbuf_adamw_hparams hp,
+                       float *__restrict__ vs, const AdamParams hp,
                        const AdamScalars hs, const float *__restrict__ total_norm,
                        const int32_t *__restrict__ nonfinite, int32_t *__restrict__ status) {
     extern __shared__ unsigned char smem_raw[];
@@ -1088,7 +1088,7 @@ __global__ void __launch_bounds__(kP8Threads, 1)
 }  // namespace
 
 int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
-                 float *exp_avg_sq, const dbuf_adamw_hparams &hp, const float *total_norm,
+                 float *exp_avg_sq, const AdamParams &hp, const float *total_norm,
                  const int32_t *nonfinite, void *stream) {
     if (p->chunks.empty()) return cudaSuccess;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1105,7 +1105,7 @@ int prepare_optim_kernels() {
 
 int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8_t *m_codes,
                   uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
-                  const dbuf_adamw_hparams &hp, const float *total_norm, const int32_t *nonfinite,
+                  const AdamParams &hp, const float *total_norm, const int32_t *nonfinite,
                   void *stream) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The pipelined kernel takes the tensors with tensor maps when every buffer

@@ -63,8 +63,8 @@ class DbufError(RuntimeError):
 
 class dbuf_adamw_hparams(ctypes.Structure):
     _fields_ = [(name, ctypes.c_float) for name in
-                ("lr", "beta1", "beta2", "eps", "weight_decay", "bias_correction1",
-                 "bias_correction2", "max_norm")]
+                ("lr", "beta1", "beta2", "eps", "weight_decay", "max_norm")] + \
+               [("step", ctypes.c_int64)]
 
 
 class dbuf_tensor_spec(ctypes.Structure):
@@ -245,13 +245,12 @@ def dbuf_block_quant(plan: int, buf: int, codes: int, scales: int, stream: int =
 
 
 def dbuf_adamw_step(plan: int, params: int, grads: int, exp_avg: int, exp_avg_sq: int, *,
-                    lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
-                    bias_correction1: float, bias_correction2: float, max_norm: float = 0.0,
-                    total_norm: int = 0, nonfinite: int = 0, stream: int = 0) -> None:
-    """One AdamW step over the tensor ranges; total_norm / nonfinite are optional
-    device pointers (0 = not given)."""
-    hp = dbuf_adamw_hparams(lr, beta1, beta2, eps, weight_decay, bias_correction1,
-                            bias_correction2, max_norm)
+                    step: int, lr: float, beta1: float, beta2: float, eps: float,
+                    weight_decay: float, max_norm: float = 0.0, total_norm: int = 0,
+                    nonfinite: int = 0, stream: int = 0) -> None:
+    """One AdamW step (step >= 1) over the tensor ranges; total_norm / nonfinite
+    are optional device pointers (0 = not given)."""
+    hp = dbuf_adamw_hparams(lr, beta1, beta2, eps, weight_decay, max_norm, step)
     _check(_lib_handle().dbuf_adamw_step(plan, params, grads, exp_avg, exp_avg_sq,
                                          ctypes.byref(hp), total_norm or None, nonfinite or None,
                                          stream), "dbuf_adamw_step")
@@ -268,14 +267,13 @@ def dbuf_plan_state_offsets(plan: int, n: int):
 
 def dbuf_adamw8_step(plan: int, params: int, grads: int, exp_avg_codes: int,
                      exp_avg_sq_codes: int, exp_avg_scales: int, exp_avg_sq_scales: int,
-                     exp_avg_fp32: int, exp_avg_sq_fp32: int, *, lr: float, beta1: float,
-                     beta2: float, eps: float, weight_decay: float, bias_correction1: float,
-                     bias_correction2: float, max_norm: float = 0.0, total_norm: int = 0,
-                     nonfinite: int = 0, stream: int = 0) -> None:
-    """One 8-bit AdamW step (block-quantised moments); pointers as in dbuf.h,
-    0 for the optional ones."""
-    hp = dbuf_adamw_hparams(lr, beta1, beta2, eps, weight_decay, bias_correction1,
-                            bias_correction2, max_norm)
+                     exp_avg_fp32: int, exp_avg_sq_fp32: int, *, step: int, lr: float,
+                     beta1: float, beta2: float, eps: float, weight_decay: float,
+                     max_norm: float = 0.0, total_norm: int = 0, nonfinite: int = 0,
+                     stream: int = 0) -> None:
+    """One 8-bit AdamW step (step >= 1, block-quantised moments); pointers as in
+    dbuf.h, 0 for the optional ones."""
+    hp = dbuf_adamw_hparams(lr, beta1, beta2, eps, weight_decay, max_norm, step)
     _check(_lib_handle().dbuf_adamw8_step(plan, params, grads, exp_avg_codes or None,
                                           exp_avg_sq_codes or None, exp_avg_scales or None,
                                           exp_avg_sq_scales or None, exp_avg_fp32 or None,

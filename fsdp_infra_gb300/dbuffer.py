@@ -200,17 +200,16 @@ class DBuffer:
                    eps: float = 1e-8, weight_decay: float = 0.0, max_norm: float = 0.0,
                    total_norm: Optional[torch.Tensor] = None,
                    nonfinite: Optional[torch.Tensor] = None, stream=None) -> None:
-        """One fused AdamW step over fp32 buffers of this layout (step >= 1).  The
-        bias corrections 1 - beta^step are formed in fp64 and rounded to fp32."""
+        """One fused AdamW step over fp32 buffers of this layout (step >= 1; the
+        library forms the bias corrections)."""
         for b in (params, grads, exp_avg, exp_avg_sq):
             self._check_buf(b)
             if b.dtype != torch.float32:
                 raise TypeError("AdamW buffers are float32")
         b1, b2 = betas
         _c.dbuf_adamw_step(self.handle, params.data_ptr(), grads.data_ptr(), exp_avg.data_ptr(),
-                           exp_avg_sq.data_ptr(), lr=lr, beta1=b1, beta2=b2, eps=eps,
-                           weight_decay=weight_decay, bias_correction1=1.0 - b1 ** step,
-                           bias_correction2=1.0 - b2 ** step, max_norm=max_norm,
+                           exp_avg_sq.data_ptr(), step=step, lr=lr, beta1=b1, beta2=b2,
+                           eps=eps, weight_decay=weight_decay, max_norm=max_norm,
                            total_norm=total_norm.data_ptr() if total_norm is not None else 0,
                            nonfinite=nonfinite.data_ptr() if nonfinite is not None else 0,
                            stream=self._stream(stream))
@@ -248,9 +247,8 @@ class DBuffer:
         _c.dbuf_adamw8_step(self.handle, params.data_ptr(), grads.data_ptr(),
                             state["m_codes"].data_ptr(), state["v_codes"].data_ptr(),
                             state["m_scales"].data_ptr(), state["v_scales"].data_ptr(),
-                            state["m32"].data_ptr(), state["v32"].data_ptr(), lr=lr, beta1=b1,
-                            beta2=b2, eps=eps, weight_decay=weight_decay,
-                            bias_correction1=1.0 - b1 ** step, bias_correction2=1.0 - b2 ** step,
+                            state["m32"].data_ptr(), state["v32"].data_ptr(), step=step,
+                            lr=lr, beta1=b1, beta2=b2, eps=eps, weight_decay=weight_decay,
                             max_norm=max_norm,
                             total_norm=total_norm.data_ptr() if total_norm is not None else 0,
                             nonfinite=nonfinite.data_ptr() if nonfinite is not None else 0,

@@ -260,7 +260,10 @@ int dbuf_norm_nonfinite(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
  * division; qmax = 448 for E4M3, 127 for INT8), replaced by 1.0 if not positive;
  * code = enc(x / scale) with an fp32 division: E4M3 rounds to nearest even and
  * saturates to +-448; INT8 rounds half to even and clamps to [-127, 127].
- * buf: device fp32 buffer (`total` elements).  codes: device uint8 buffer of
+ * buf: device fp32 buffer (`total` elements).  The input type is fixed: the
+ * quantiser's input on this path is the fp32 gradient accumulator (or fp32
+ * master weights), so there is no dtype argument and a bf16 buffer is not
+ * supported.  codes: device uint8 buffer of
  * `total` bytes, same layout; bytes outside quantised tensors are untouched.
  * scales: device fp32 array of n_scales entries, tensor by tensor in row-major
  * block order starting at scale_offsets[t].  Inputs with inf/NaN give
@@ -287,14 +290,16 @@ int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, 
  * DBUF_NOALLOC_SCRATCH_BYTES, about 87,000 chunks or 1.4e9 elements) is
  * rejected with DBUF_ERANGE before anything is launched.  The first call on a
  * device looks up the array's device address (once per device, with that
- * device current); make that first call before any stream capture.  All calls
- * share the one array: calls that may overlap on the GPU (other streams, other
- * host threads) race on it, so the caller must serialise them.  The counters
- * that must start at zero are zero when the library loads and every call
- * returns them to zero before it finishes; everything else a call reads it
- * writes first, so it does not depend on what the previous call left in the
- * array.  The call allocates nothing (no cudaMalloc, cudaFree or allocating
- * library routine).
+ * device current) and keeps it; make that first call before any stream
+ * capture, and do not reset the device (cudaDeviceReset) afterwards, since the
+ * kept address would then be stale.  All calls share the one array: calls that
+ * may overlap on the GPU (other streams, other host threads) race on it and
+ * their results are not valid, so the caller must serialise them.  Each call
+ * enqueues a memset of the array's completion counters on `stream` before its
+ * kernel, and everything else a call reads it writes first, so a call does not
+ * depend on what an earlier call left in the array (not even one that raced).
+ * The call allocates nothing (no cudaMalloc, cudaFree or allocating library
+ * routine).
  * Arguments, outputs and other errors as for dbuf_norm_nonfinite.
  */
 #define DBUF_NOALLOC_SCRATCH_BYTES ((size_t)1 << 20)
@@ -313,16 +318,20 @@ int dbuf_norm_nonfinite_noalloc(const dbuf_plan_t *plan, const void *buf, int32_
  */
 int dbuf_device_status(const dbuf_plan_t *plan, int32_t *status, void *stream);
 
-/* Hyperparameters of one AdamW step (host struct, copied by value). */
+/* Hyperparameters of one AdamW step (host struct, copied by value; 32 bytes).
+ * The library forms the bias corrections bc1 = 1 - beta1^step and
+ * bc2 = 1 - beta2^step itself: each power in fp64 from the fp32 beta
+ * (pow((double)beta, (double)step)), subtracted from 1 in fp64, rounded once
+ * to fp32.  The call is rejected (DBUF_EINVAL) for step < 1 or when a
+ * correction is not a positive finite fp32 value (e.g. beta = 1). */
 typedef struct dbuf_adamw_hparams {
     float lr;
     float beta1;
     float beta2;
     float eps;
-    float weight_decay;     /* decoupled: p *= 1 - lr*weight_decay */
-    float bias_correction1; /* 1 - beta1^t for step t >= 1, computed by the caller */
-    float bias_correction2; /* 1 - beta2^t */
-    float max_norm;         /* > 0: clip the gradient to this global L2 norm */
+    float weight_decay; /* decoupled: p *= 1 - lr*weight_decay */
+    float max_norm;     /* > 0: clip the gradient to this global L2 norm */
+    int64_t step;       /* t >= 1: the step being taken, counted from 1 */
 } dbuf_adamw_hparams;
 
 /*
@@ -341,8 +350,8 @@ typedef struct dbuf_adamw_hparams {
  * flag of dbuf_norm_nonfinite) is given and non-zero, the step is skipped and
  * nothing is written.  params, exp_avg, exp_avg_sq: device fp32 buffers,
  * updated in place; grads: device fp32 buffer (e.g. the accumulator).  Padding
- * is untouched.  Errors: DBUF_EINVAL (null pointers, non-positive bias
- * corrections), DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ * is untouched.  Errors: DBUF_EINVAL (null pointers, step < 1, a bias
+ * correction that is not positive), DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
  */
 int dbuf_adamw_step(const dbuf_plan_t *plan, float *params, const float *grads, float *exp_avg,
                     float *exp_avg_sq, const dbuf_adamw_hparams *hp, const float *total_norm,
@@ -388,8 +397,8 @@ int dbuf_plan_state_offsets(const dbuf_plan_t *plan, int64_t *state_offsets, int
  *     n_state is 0).
  * hp, total_norm and nonfinite as for dbuf_adamw_step (clipping from a device
  * norm; a set non-finite flag skips the step and nothing is written).
- * Errors: DBUF_EINVAL (null pointers, non-positive bias corrections),
- * DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ * Errors: DBUF_EINVAL (null pointers, step < 1, a bias correction that is
+ * not positive), DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
  */
 int dbuf_adamw8_step(const dbuf_plan_t *plan, float *params, const float *grads,
                      uint8_t *exp_avg_codes, uint8_t *exp_avg_sq_codes, float *exp_avg_scales,

@@ -80,14 +80,16 @@ def lib():
         f = ctypes.c_float
         L.orc_clip_coef.argtypes = [f, f]
         L.orc_clip_coef.restype = f
-        L.orc_adamw.argtypes = [i32, P, P, P, P, P, P, f, f, f, f, f, f, f, f, f, i32]
+        L.orc_bias_correction.argtypes = [f, i64]
+        L.orc_bias_correction.restype = f
+        L.orc_adamw.argtypes = [i32, P, P, P, P, P, P, f, f, f, f, f, i64, f, f, i32]
         L.orc_adamw.restype = None
         L.orc_v_code.argtypes = [f, f]
         L.orc_v_code.restype = ctypes.c_uint8
         L.orc_state_offsets.argtypes = [i32, P, P, P]
         L.orc_state_offsets.restype = ctypes.c_int64
         L.orc_adamw8.argtypes = [i32, P, P, P, P, P, P, P, P, P, P, P, P, P, P, P,
-                                 f, f, f, f, f, f, f, f, f, i32]
+                                 f, f, f, f, f, i64, f, f, i32]
         L.orc_adamw8.restype = None
         for fn in ("orc_gather", "orc_scatter"):
             getattr(L, fn).argtypes = [i32, P, P, i32, P, P, i32, P]
@@ -250,15 +252,21 @@ def clip_coef(max_norm: float, total_norm: float) -> float:
     return float(lib().orc_clip_coef(max_norm, total_norm))
 
 
+def bias_correction(beta: float, step: int) -> float:
+    """1 - beta^step as the optimizer steps use it (fp64 power of the fp32 beta,
+    rounded to fp32)."""
+    return float(lib().orc_bias_correction(beta, int(step)))
+
+
 def adamw(p: Plan, params: np.ndarray, grad: np.ndarray, m: np.ndarray, v: np.ndarray, *,
           lr: float, beta1: float, beta2: float, eps: float, weight_decay: float,
-          bc1: float, bc2: float, max_norm: float = 0.0, total_norm: float = 0.0,
+          step: int, max_norm: float = 0.0, total_norm: float = 0.0,
           nonfinite: int = 0) -> None:
-    """One AdamW step over the tensor ranges (in place on params, m, v)."""
+    """One AdamW step (step t >= 1) over the tensor ranges (in place on params, m, v)."""
     for a in (params, grad, m, v):
         assert a.dtype == np.float32 and a.flags["C_CONTIGUOUS"]
     lib().orc_adamw(len(p.offsets), _p(p.offsets), _p(_i64(p.numel)), _p(params), _p(grad),
-                    _p(m), _p(v), lr, beta1, beta2, eps, weight_decay, bc1, bc2, max_norm,
+                    _p(m), _p(v), lr, beta1, beta2, eps, weight_decay, int(step), max_norm,
                     total_norm, int(nonfinite))
 
 
@@ -282,7 +290,7 @@ def state_offsets(specs):
 def adamw8(p: Plan, specs, params: np.ndarray, grad: np.ndarray, m_codes: np.ndarray,
            v_codes: np.ndarray, m_scales: np.ndarray, v_scales: np.ndarray, m32: np.ndarray,
            v32: np.ndarray, *, lr: float, beta1: float, beta2: float, eps: float,
-           weight_decay: float, bc1: float, bc2: float, max_norm: float = 0.0,
+           weight_decay: float, step: int, max_norm: float = 0.0,
            total_norm: float = 0.0, nonfinite: int = 0) -> None:
     """One 8-bit AdamW step (in place): INT8 block moments (codes in the flat
     buffer's layout, one fp32 scale per block) for quantised tensors, compact
@@ -300,7 +308,7 @@ def adamw8(p: Plan, specs, params: np.ndarray, grad: np.ndarray, m_codes: np.nda
     assert m_codes.size >= p.total and v_codes.size >= p.total and params.size >= p.total
     lib().orc_adamw8(n, _p(p.offsets), _p(r), _p(c), _p(qr), _p(qc), _p(q), _p(so), _p(params),
                      _p(grad), _p(m_codes), _p(v_codes), _p(m_scales), _p(v_scales), _p(m32),
-                     _p(v32), lr, beta1, beta2, eps, weight_decay, bc1, bc2, max_norm,
+                     _p(v32), lr, beta1, beta2, eps, weight_decay, int(step), max_norm,
                      total_norm, int(nonfinite))
 
 

@@ -456,6 +456,16 @@ float orc_clip_coef(float max_norm, float total_norm)
     return c < 1.0f ? c : 1.0f;
 }
 
+/* Bias correction 1 - beta^t of Adam's moment estimates for step t >= 1: the
+ * power of the fp32 beta taken in fp64 by the C library's pow, subtracted from
+ * 1 in fp64, rounded once to fp32 (the reading of this library: the pages give
+ * no formula). */
+float orc_bias_correction(float beta, int64_t step)
+{
+    double c = 1.0 - pow((double)beta, (double)step);
+    return (float)c;
+}
+
 /* One AdamW step with decoupled weight decay over every tensor range of the
  * flat buffer [veScale-3, OpDispatcher: fused AdamW handler on the local shard;
  * veScale-FSDP, §5 DBuffer group-level operators].  The pages name the fused
@@ -464,15 +474,17 @@ float orc_clip_coef(float max_norm, float total_norm)
  *   g = grad * coef;  p = p * (1 - lr*wd)
  *   m = beta1*m + (1-beta1)*g;  v = beta2*v + ((1-beta2)*g)*g
  *   p = p - (lr/bc1) * (m / (sqrt(v / bc2) + eps))
- * with bc1 = 1 - beta1^t and bc2 = 1 - beta2^t given by the caller.  When
+ * with bc1 = 1 - beta1^t and bc2 = 1 - beta2^t for step t (orc_bias_correction).  When
  * `nonfinite` is non-zero the step is skipped (nothing is written), as a
  * gradient scaler skips a step with inf/NaN gradients. */
 void orc_adamw(int32_t n, const int64_t *offsets, const int64_t *numel, float *p,
                const float *grad, float *m, float *v, float lr, float beta1, float beta2,
-               float eps, float wd, float bc1, float bc2, float max_norm, float total_norm,
+               float eps, float wd, int64_t step, float max_norm, float total_norm,
                int32_t nonfinite)
 {
     if (nonfinite) return;
+    float bc1 = orc_bias_correction(beta1, step);
+    float bc2 = orc_bias_correction(beta2, step);
     orc_adamw_scalars s;
     s.coef = orc_clip_coef(max_norm, total_norm);
     s.decay = 1.0f - lr * wd;
@@ -540,10 +552,12 @@ void orc_adamw8(int32_t n, const int64_t *offsets, const int64_t *rows, const in
                 const int64_t *qrows, const int64_t *qcols, const int32_t *quant,
                 const int64_t *state_offsets, float *p, const float *grad, uint8_t *m_codes,
                 uint8_t *v_codes, float *m_scales, float *v_scales, float *m32, float *v32,
-                float lr, float beta1, float beta2, float eps, float wd, float bc1, float bc2,
+                float lr, float beta1, float beta2, float eps, float wd, int64_t step,
                 float max_norm, float total_norm, int32_t nonfinite)
 {
     if (nonfinite) return;
+    float bc1 = orc_bias_correction(beta1, step);
+    float bc2 = orc_bias_correction(beta2, step);
     orc_adamw_scalars s;
     s.coef = orc_clip_coef(max_norm, total_norm);
     s.decay = 1.0f - lr * wd;

@@ -67,9 +67,9 @@ def test_operators_refuse_unuploaded_plan_without_gpu(dbuf_lib):
                      lambda: d.dbuf_scale_accum_zero(p, 0, d.DBUF_F32, 0, 0.5),
                      lambda: d.dbuf_norm_nonfinite(p, 0, d.DBUF_F32, 0, 0, 0, 0, 0),
                      lambda: d.dbuf_block_quant(p, 0, 0, 0),
-                     lambda: d.dbuf_adamw8_step(p, 0, 0, 0, 0, 0, 0, 0, 0, lr=1e-3, beta1=0.9,
-                                                beta2=0.95, eps=1e-8, weight_decay=0.0,
-                                                bias_correction1=0.1, bias_correction2=0.05),
+                     lambda: d.dbuf_adamw8_step(p, 0, 0, 0, 0, 0, 0, 0, 0, step=1, lr=1e-3,
+                                                beta1=0.9, beta2=0.95, eps=1e-8,
+                                                weight_decay=0.0),
                      lambda: d.dbuf_gather(p, 0, d.DBUF_F32, 0),
                      lambda: d.dbuf_scatter(p, 0, d.DBUF_F32, 0),
                      lambda: d.dbuf_selftest_wait_timeout(p, 100)]:
@@ -96,3 +96,24 @@ def test_product_path_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(d, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         d.library()
+
+
+def test_adamw_rejects_bad_step_and_betas_without_gpu(dbuf_lib):
+    """The library forms 1 - beta^t itself: step < 1, or a beta that makes a
+    correction zero, is refused before the plan is even looked at."""
+    d = dbuf_lib
+    p = d.dbuf_plan([(8, 8, 1)], 2)
+    try:
+        kw = dict(lr=1e-3, beta1=0.9, beta2=0.95, eps=1e-8, weight_decay=0.0)
+        for bad in [dict(kw, step=0), dict(kw, step=-3), dict(kw, step=1, beta1=1.0),
+                    dict(kw, step=5, beta2=1.0)]:
+            for call in (lambda: d.dbuf_adamw_step(p, 0, 0, 0, 0, **bad),
+                         lambda: d.dbuf_adamw8_step(p, 0, 0, 0, 0, 0, 0, 0, 0, **bad)):
+                with pytest.raises(d.DbufError) as e:
+                    call()
+                assert e.value.code == d.DBUF_EINVAL
+        with pytest.raises(d.DbufError) as e:
+            d.dbuf_adamw_step(p, 0, 0, 0, 0, step=1, **kw)
+        assert e.value.code == d.DBUF_ENOTUPLOADED
+    finally:
+        d.dbuf_plan_free(p)

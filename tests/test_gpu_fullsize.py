@@ -254,9 +254,8 @@ def test_next_rows_beyond_32bit_offsets(dbuf_lib, oracle_lib):
     hp = dict(lr=1e-3, betas=(0.9, 0.95), eps=1e-8, weight_decay=0.1)
     b1, b2 = hp["betas"]
     step, max_norm, total = 3, 0.5, 0.75
-    bc1, bc2 = float(np.float32(1 - b1 ** step)), float(np.float32(1 - b2 ** step))
     okw = dict(lr=hp["lr"], beta1=b1, beta2=b2, eps=hp["eps"], weight_decay=hp["weight_decay"],
-               bc1=bc1, bc2=bc2, max_norm=max_norm, total_norm=total)
+               step=step, max_norm=max_norm, total_norm=total)
 
     gen = torch.Generator(device=DEV)
     gen.manual_seed(31)

@@ -38,8 +38,7 @@ def _oracle_step(oracle_lib, op, host, step, max_norm=0.0, total=0.0, flag=0):
     b1, b2 = HP["betas"]
     oracle_lib.adamw(op, host["p"], host["g"], host["m"], host["v"], lr=HP["lr"], beta1=b1,
                      beta2=b2, eps=HP["eps"], weight_decay=HP["weight_decay"],
-                     bc1=float(np.float32(1.0 - b1 ** step)), bc2=float(np.float32(1.0 - b2 ** step)),
-                     max_norm=max_norm, total_norm=total, nonfinite=flag)
+                     step=step, max_norm=max_norm, total_norm=total, nonfinite=flag)
 
 
 def _run_steps(oracle_lib, specs, m, steps, units=None, align=16, shift=0):

@@ -107,8 +107,7 @@ class Case:
         h = self.h
         self.ol.adamw8(self.op, self.specs, h["p"], g, h["mc"], h["vc"], h["ms"], h["vs"],
                        h["m32"], h["v32"], lr=hp["lr"], beta1=b1, beta2=b2, eps=hp["eps"],
-                       weight_decay=hp["weight_decay"], bc1=float(np.float32(1 - b1 ** step)),
-                       bc2=float(np.float32(1 - b2 ** step)), max_norm=max_norm,
+                       weight_decay=hp["weight_decay"], step=step, max_norm=max_norm,
                        total_norm=total32, nonfinite=1 if skip else 0)
         torch.cuda.synchronize()
         for k in h:
@@ -196,8 +195,8 @@ def test_adamw8_dense7b_layer_full_size(dbuf_lib, oracle_lib):
         v32 = np.zeros(max(nst1, 1), np.float32)
         oracle_lib.adamw8(sp, [s], hp_, grads[t].numpy().copy(), mc, vc, ms, vs, m32, v32,
                           lr=HP["lr"], beta1=b1, beta2=b2, eps=HP["eps"],
-                          weight_decay=HP["weight_decay"], bc1=float(np.float32(1 - b1 ** 3)),
-                          bc2=float(np.float32(1 - b2 ** 3)), max_norm=0.5, total_norm=0.75)
+                          weight_decay=HP["weight_decay"], step=3, max_norm=0.5,
+                          total_norm=0.75)
         assert_bits_equal(f32(p[o:o + k]), hp_, f"params t{t}")
         if s.quant:
             assert np.array_equal(st["m_codes"][o:o + k].cpu().numpy(), mc), f"m codes t{t}"

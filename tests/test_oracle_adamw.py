@@ -49,10 +49,8 @@ def test_adamw_matches_torch(oracle_lib):
             grad[int(o):int(o) + s.numel] = g
             tp.grad = torch.from_numpy(g.copy())
         opt.step()
-        bc1 = np.float32(1.0 - b1 ** step)
-        bc2 = np.float32(1.0 - b2 ** step)
         oracle_lib.adamw(p, params, grad, m, v, lr=lr, beta1=b1, beta2=b2, eps=eps,
-                         weight_decay=wd, bc1=float(bc1), bc2=float(bc2))
+                         weight_decay=wd, step=step)
     got = _gather(p, params, specs)
     want = np.concatenate([t.detach().numpy() for t in tparams])
     # the update is lr-sized: differences of rounding order stay far below it
@@ -74,7 +72,7 @@ def test_adamw_skip_zero_lr_and_padding(oracle_lib):
     m = rng.standard_normal(p.total).astype(np.float32)
     v = np.abs(rng.standard_normal(p.total)).astype(np.float32)
     ref = [a.copy() for a in (params, grad, m, v)]
-    kw = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, bc1=0.1, bc2=0.001)
+    kw = dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1)
     oracle_lib.adamw(p, params, grad, m, v, nonfinite=1, **kw)          # skipped step
     for a, r in zip((params, grad, m, v), ref):
         assert np.array_equal(a.view(np.uint32), r.view(np.uint32))
@@ -100,7 +98,7 @@ def test_adamw_zero_betas_states_are_g_and_g_squared(oracle_lib):
     m = np.full(p.total, 7.0, np.float32)
     v = np.full(p.total, 7.0, np.float32)
     oracle_lib.adamw(p, params, grad, m, v, lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8,
-                     weight_decay=0.0, bc1=1.0, bc2=1.0)
+                     weight_decay=0.0, step=1)
     assert np.array_equal(m[o:o + 500], g)
     assert np.array_equal(v[o:o + 500], g * g)
 
@@ -122,7 +120,7 @@ def test_adamw_first_step_closed_form(oracle_lib):
     v = np.zeros(p.total, np.float32)
     b1, b2 = 0.9, 0.999
     oracle_lib.adamw(p, params, grad, m, v, lr=lr, beta1=b1, beta2=b2, eps=1e-8, weight_decay=wd,
-                     bc1=1 - b1, bc2=1 - b2)
+                     step=1)
     want = p0.astype(np.float64) * (1 - lr * wd) - lr * np.sign(g)
     assert np.max(np.abs(params[o:o + 300] - want)) < 1e-6
 

@@ -77,8 +77,7 @@ def _grad(p, specs, rng, std=1e-3):
 def _step8(oracle_lib, p, specs, st, g, step, **kw):
     b1, b2 = HP["beta1"], HP["beta2"]
     oracle_lib.adamw8(p, specs, st["p"], g, st["mc"], st["vc"], st["ms"], st["vs"], st["m32"],
-                      st["v32"], **HP, bc1=float(np.float32(1 - b1 ** step)),
-                      bc2=float(np.float32(1 - b2 ** step)), **kw)
+                      st["v32"], **HP, step=step, **kw)
 
 
 def test_v_code_is_the_nearest_nonzero_level(oracle_lib):
@@ -140,8 +139,7 @@ def test_adamw8_is_dequantise_adamw_requantise(oracle_lib):
         m[o:o + s.numel] = mm.reshape(-1)
         v[o:o + s.numel] = vv.reshape(-1)
     pw = st["p"].copy()
-    oracle_lib.adamw(p, pw, g, m, v, **HP, bc1=float(np.float32(1 - 0.9 ** 4)),
-                     bc2=float(np.float32(1 - 0.95 ** 4)), max_norm=0.05, total_norm=0.2)
+    oracle_lib.adamw(p, pw, g, m, v, **HP, step=4, max_norm=0.05, total_norm=0.2)
     int8_specs = [TensorSpec(s.name, s.rows, s.cols, s.gran_rows, s.qblock, "int8" if s.quant else None)
                   for s in specs]
     want_mc = np.zeros(p.total, np.uint8)
@@ -178,7 +176,7 @@ def test_adamw8_first_step_closed_form(oracle_lib):
     # exactly as the fp32 step from zero moments
     pw = st["p"].copy()
     oracle_lib.adamw(p, pw, g, np.zeros(p.total, np.float32), np.zeros(p.total, np.float32), **HP,
-                     bc1=float(np.float32(0.1)), bc2=float(np.float32(0.05)))
+                     step=1)
     _step8(oracle_lib, p, specs, st, g, 1)
     for t, (o, s) in enumerate(zip(p.offsets, specs)):
         sl = slice(int(o), int(o) + s.numel)
@@ -237,8 +235,7 @@ def test_adamw8_tracks_the_fp32_step(oracle_lib):
     for step in range(1, 31):
         g = _grad(p, specs, rng)
         _step8(oracle_lib, p, specs, st, g, step)
-        oracle_lib.adamw(p, p32, g, m, v, **HP, bc1=float(np.float32(1 - 0.9 ** step)),
-                         bc2=float(np.float32(1 - 0.95 ** step)))
+        oracle_lib.adamw(p, p32, g, m, v, **HP, step=step)
     travel = np.abs(p32 - p0)
     dev = np.abs(st["p"] - p32)
     assert np.max(dev) <= 0.5 * 30 * HP["lr"]
