@@ -404,7 +404,10 @@ def run_reference(args):
             "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(1000 * total / args.steps, 3), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": _config_dict(None, "dense7b"),
+            "config": _reference_config(),
+            "note": ("the oracle's rate per algorithmic byte on a bounded sample of the 7B "
+                     "stack; a ratio against the GPU line compares per-byte rates, the "
+                     "workloads differ in size"),
             "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1,
                              "kind": "oracle", "sample": desc,
                              "ops_gbs": getattr(oracle_sample_pass, "last_ops", None),
@@ -413,6 +416,19 @@ def run_reference(args):
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
     return 0
+
+
+def _reference_config():
+    """The workload the reference arm times: one slice of the dense stack."""
+    from workloads import workload
+    w = workload("dense7b")
+    emb = w.groups[1].tensors[0]
+    return {"workload": (f"{REF_SAMPLE_ROWS}x{emb.cols} slice of the 7B-shaped stack's "
+                         f"{emb.rows}x{emb.cols} embedding table planned as one DBuffer "
+                         f"(m={w.m}, 128x128 E4M3 blocks, s=1/{w.m}): pack_cast, unpack, "
+                         "scale_accum_zero, norm_nonfinite, block_quant, once per step"),
+            "key": "dense7b_embedding_slice", "elements_per_step": REF_SAMPLE_ROWS * emb.cols,
+            "m": w.m, "sample_of": "dense7b"}
 
 
 def _config_dict(stack, key):
@@ -496,6 +512,77 @@ def op_alone_ms(stack, op, eager, passes=3, min_launches=32):
     e.record()
     torch.cuda.synchronize()
     return s.elapsed_time(e) / (passes * reps)
+
+
+def step_alone_ms(stack, eager, passes=3, min_steps=32):
+    """Milliseconds of one whole step (every operator over every DBuffer), timed
+    like op_alone_ms: a workload of few DBuffers repeats its step inside one
+    graph until it holds at least `min_steps` DBuffer steps."""
+    reps = max(1, -(-min_steps // max(1, len(stack.dbufs))))
+
+    def one():
+        for _ in range(reps):
+            stack.step()
+
+    graph = None
+    if not eager:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            one()
+    run = graph.replay if graph is not None else one
+    run()
+    torch.cuda.synchronize()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(passes):
+        run()
+    e.record()
+    torch.cuda.synchronize()
+    return s.elapsed_time(e) / (passes * reps)
+
+
+PER_CONFIG = ("tiny", "llama_layer", "moe", "mixed")
+
+
+def run_per_config(args, device, peak):
+    """The other four workloads, each planned and stepped alone on this GPU
+    (outside the timed region of the headline step): per operator its launches
+    back to back in one graph (at least 32 launches, 3 passes), and the whole
+    step the same way.  GB/s = algorithmic bytes (tensor ranges only) / time;
+    elements/s = the workload's elements / time."""
+    from workloads import workload
+    out = {}
+    for key in PER_CONFIG:
+        w = workload(key)
+        st = Stack(w, device)
+        torch.cuda.synchronize()
+        for _ in range(max(args.warmup, 1)):
+            st.step()
+        torch.cuda.synchronize()
+        ops = {}
+        for op in ("pack_cast", "unpack", "scale_accum_zero", "norm_nonfinite", "block_quant"):
+            if st.op_bytes.get(op, 0) == 0:
+                continue
+            ms = op_alone_ms(st, op, args.eager)
+            gbs = st.op_bytes[op] / (ms / 1e3) / 1e9
+            ops[op] = {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                       "elements_per_s": round(st.elements / (ms / 1e3), 1)}
+        ms = step_alone_ms(st, args.eager)
+        gbs = st.bytes_per_step / (ms / 1e3) / 1e9
+        l2 = w.total_numel * 4 > 2 * 129e6
+        out[key] = {"workload": w.description, "m": w.m, "dbuffers": len(st.dbufs),
+                    "elements": st.elements, "bytes_per_step": st.bytes_per_step,
+                    "grad_dtype": "bf16" if w.grad_dtype == torch.bfloat16 else "f32",
+                    "l2": ("buffers larger than L2 (129 MB)" if l2 else
+                           "L2-resident small case: figures are L2 rates, not HBM"),
+                    "step": {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
+                             "elements_per_s": round(st.elements / (ms / 1e3), 1)},
+                    "ops": ops}
+        for d in st.dbufs:
+            d["kind"]["db"].close()
+        del st
+        torch.cuda.empty_cache()
+    return out
 
 
 def run_ours(args):
@@ -619,6 +706,11 @@ def run_ours(args):
     # ---- end to end: host inputs (pinned) -> device, operators, results -> host
     e2e = None if args.no_e2e else run_e2e(stack, args, world)
 
+    # ---- the other workloads, each alone (not part of the timed step)
+    per_config = None
+    if not args.no_per_config and args.workload == "dense7b":
+        per_config = run_per_config(args, device, peak)
+
     line = None
     if rank == 0:
         cpu = None
@@ -628,6 +720,7 @@ def run_ours(args):
             gbs, eps, dt, desc = oracle_sample_pass(1)
             cpu = {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                    "sample": desc, "seconds": round(dt, 2),
+                   "note": "per-byte rate on a bounded sample, not the whole step",
                    "ops_gbs": getattr(oracle_sample_pass, "last_ops", None),
                    "host": _host_cpu()}
         line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -649,7 +742,12 @@ def run_ours(args):
                              (f" (each pass repeated {-(-32 // len(stack.dbufs))}x, "
                               "at least 32 launches)" if len(stack.dbufs) < 32 else "") +
                              "; evented_*: one step with events around every launch"),
-                "clocks": clock_info, "ops": ops}
+                "clocks": clock_info, "ops": ops, "per_config": per_config,
+                "per_config_note": ("each workload planned and stepped alone after the timed "
+                                    "region: per operator its launches back to back in one "
+                                    "graph (at least 32 launches, 3 passes); step = all five "
+                                    "operators, timed the same way; frac of the measured "
+                                    "copy peak")}
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -959,6 +1057,7 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of as one CUDA graph")
     ap.add_argument("--workload", default="dense7b",

@@ -29,7 +29,9 @@ def test_reference_arm_prints_one_line(oracle_lib):
     assert d["impl"] == "reference"
     assert d["value"] > 0 and d["unit"] == "GB/s" and d["higher_is_better"] is True
     assert d["steps"] == 1 and d["warmup"] == 0
-    assert d["config"]["key"] == "dense7b"
+    # the config names the sample the oracle actually runs, a slice of the 7B stack
+    assert d["config"]["key"] == "dense7b_embedding_slice"
+    assert d["config"]["sample_of"] == "dense7b" and "slice" in d["config"]["workload"]
     cpu = d["cpu_baseline"]
     assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and cpu["value"] == d["value"]
     assert cpu["sample"]
