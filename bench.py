@@ -13,9 +13,12 @@ quantisation, s = 1/64): per DBuffer
 Throughput = algorithmic bytes (tensor ranges only, padding excluded) / time.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                       [--exchange]
 N>1 runs under torch.distributed.run: one independent replica per GPU (the path
-has no exchange step on one GPU), timing max over ranks.  --impl reference times
-the CPU oracle on a bounded sample of the same workload (rank 0 only).
+has no exchange step on one GPU), timing max over ranks.  --exchange instead runs
+the sharded step with its collectives, each DBuffer planned with m = N.  --impl
+reference times the CPU oracle on a bounded sample of the same workload (rank 0
+only).
 """
 from __future__ import annotations
 
@@ -755,6 +758,111 @@ def run_ours(args):
     return 0
 
 
+def run_exchange(args):
+    """--exchange: the data-parallel step with its collectives, one rank per GPU
+    (fsdp_infra_gb300.exchange.ShardedStep).  Every DBuffer of the workload is
+    re-planned with m = world size (an even plan, one slice per rank); a step runs,
+    for every DBuffer, copy-in of the rank's gradients, ReduceScatter, the slice's
+    scale/accumulate/zero, sharded norm (AllReduce of the partial sums and the
+    flag) and block quantisation, then the cast of the rank's master pieces,
+    AllGather and copy-out.  Launched eagerly; the step time includes the
+    collectives.  `value` counts the group operators' algorithmic bytes of every
+    rank (full-buffer pack and unpack, slice sac, norm and quantisation);
+    `collective_bytes_per_rank` the bytes each rank sends into the collectives.
+    With one GPU the process group has one rank and the collectives copy."""
+    import torch.distributed as dist
+    from fsdp_infra_gb300 import DBuffer
+    from fsdp_infra_gb300.exchange import ShardedStep
+    from workloads import workload, param_values
+    rank, world, local = _dist()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=device)
+    else:
+        import socket
+        with socket.socket() as sk:
+            sk.bind(("127.0.0.1", 0))
+            port = sk.getsockname()[1]
+        dist.init_process_group("nccl", init_method=f"tcp://127.0.0.1:{port}", rank=0,
+                                world_size=1, device_id=device)
+    w = workload(args.workload)
+    peak, peak_kind = _peaks()
+    kinds, items = [], []
+    for gi, g in enumerate(w.groups):
+        full = DBuffer(g.tensors, world, None, w.align, device=device).upload()
+        loc = full.slice(rank).upload()
+        k = {"full": full, "local": loc, "step": ShardedStep(full, loc, rank, world),
+             "grad_full": torch.zeros(full.total, dtype=torch.float32, device=device),
+             "grad_local": torch.zeros(loc.total, dtype=torch.float32, device=device),
+             "acc_local": torch.zeros(loc.total, dtype=torch.float32, device=device),
+             "buf_local": torch.zeros(loc.total, dtype=torch.bfloat16, device=device),
+             "buf_full": torch.zeros(full.total, dtype=torch.bfloat16, device=device),
+             "codes": torch.zeros(max(loc.total, 1), dtype=torch.uint8, device=device),
+             "scales": torch.zeros(max(loc.n_scales, 1), dtype=torch.float32, device=device)}
+        kinds.append(k)
+        for r in range(g.repeat):
+            master = [param_values(w, gi, t, device=device, seed=1000 * r + gi)
+                      for t in range(len(g.tensors))]
+            gen = torch.Generator(device=device)
+            gen.manual_seed(4321 + 97 * rank + r)
+            grads = [torch.randn(s.rows, s.cols, generator=gen, device=device).mul_(w.grad_std)
+                     for s in g.tensors]
+            compute = [torch.empty(s.rows, s.cols, dtype=torch.bfloat16, device=device)
+                       for s in g.tensors]
+            for x in (master, grads, compute):
+                full.ptr_table(x)
+            items.append((k, master, grads, compute))
+
+    def step():
+        for k, master, grads, compute in items:
+            k["step"].reduce_gradients(grads, k["grad_full"], k["grad_local"], k["acc_local"],
+                                       1.0 / world, codes=k["codes"], scales=k["scales"])
+            k["step"].gather_parameters(master, k["buf_local"], k["buf_full"], compute)
+
+    for _ in range(max(args.warmup, 1)):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clocks = ClockSampler(device)
+    clocks.start()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    clock_info = clocks.stop()
+    ms = max_over_ranks(s.elapsed_time(e), device) / args.steps
+    op_bytes, coll = 0, 0
+    for k, master, grads, compute in items:
+        full, loc = k["full"], k["local"]
+        E = sum(full.numel)
+        qe = sum(n for n, sp in zip(loc.piece_numels, full.specs) if sp.quant)
+        el = sum(loc.piece_numels)
+        op_bytes += 8 * E + 4 * E          # copy-in fp32 -> fp32, copy-out bf16 -> bf16
+        op_bytes += 16 * el + 4 * el + 6 * el + 5 * qe + 4 * loc.n_scales  # sac, norm, cast, quant
+        coll += 4 * full.total + 2 * loc.total + 16 * full.n
+    value = world * op_bytes / (ms / 1e3) / 1e9
+    if rank == 0:
+        line = {"metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+                "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic", "mode": "exchange",
+                "config": dict(_config_dict(None, args.workload), m=world,
+                               parallelism=f"fsdp{world} (one shard slice per rank)"),
+                "collective_bytes_per_rank": coll, "op_bytes_per_rank": op_bytes,
+                "frac_of_peak": round(value / world / peak, 4), "peak_kind": peak_kind,
+                "launch": "eager, collectives on the default stream", "clocks": clock_info}
+        print(json.dumps(line), flush=True)
+    for k in kinds:
+        k["local"].close()
+        k["full"].close()
+    dist.destroy_process_group()
+    return 0
+
+
 def run_adamw(stack, args, world, peak, barrier):
     """The fused AdamW step (dbuf_adamw_step) over every DBuffer of the workload:
     fp32 master parameters, the accumulated gradients and both moments in the
@@ -1058,6 +1166,9 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-adamw", action="store_true")
     ap.add_argument("--no-per-config", action="store_true")
+    ap.add_argument("--exchange", action="store_true",
+                    help="the sharded step with its collectives (m = number of GPUs) instead "
+                         "of independent replicas of the group-operator pass")
     ap.add_argument("--eager", action="store_true",
                     help="launch the timed steps one by one instead of as one CUDA graph")
     ap.add_argument("--workload", default="dense7b",
@@ -1067,6 +1178,8 @@ def main():
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.exchange:
+        return run_exchange(args)
     return run_ours(args)
 
 

@@ -177,6 +177,29 @@ extern "C" int dbuf_norm_nonfinite(const dbuf_plan_t *p, const void *buf, int32_
                                     stream));
 }
 
+extern "C" int dbuf_norm_sumsq(const dbuf_plan_t *p, const void *buf, int32_t dtype,
+                               double *tensor_sumsq, int32_t *nonfinite, void *workspace,
+                               size_t workspace_bytes, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!dtype_ok(dtype)) return DBUF_EINVAL;
+    if (!nonfinite || !workspace) return DBUF_EINVAL;
+    if (p->n > 0 && (!buf || !tensor_sumsq)) return DBUF_EINVAL;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DBUF_EINVAL;
+    if (workspace_bytes < dbuf::norm_workspace_bytes(p)) return DBUF_EINVAL;
+    return finish(dbuf::launch_norm(p, buf, dtype, nullptr, nullptr, nonfinite, workspace, stream,
+                                    tensor_sumsq));
+}
+
+extern "C" int dbuf_norm_finish(const dbuf_plan_t *p, const double *tensor_sumsq,
+                                float *tensor_norms, float *total_norm, void *stream) {
+    int rc = check_plan(p);
+    if (rc) return rc;
+    if (!total_norm) return DBUF_EINVAL;
+    if (p->n > 0 && (!tensor_sumsq || !tensor_norms)) return DBUF_EINVAL;
+    return finish(dbuf::launch_norm_finish(p, tensor_sumsq, tensor_norms, total_norm, stream));
+}
+
 extern "C" int dbuf_block_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes,
                                 float *scales, void *stream) {
     int rc = check_plan(p);
@@ -248,6 +271,7 @@ extern "C" int dbuf_adamw8_step(const dbuf_plan_t *p, float *params, const float
 
 extern "C" int dbuf_gather(const dbuf_plan_t *p, void *const *shards, int32_t dtype,
                            void *const *dst, void *stream) {
+    if (p && p->slice_k >= 0) return DBUF_EINVAL;  // needs every shard
     int rc = check_plan(p);
     if (rc) return rc;
     if (!dtype_ok(dtype)) return DBUF_EINVAL;
@@ -257,6 +281,7 @@ extern "C" int dbuf_gather(const dbuf_plan_t *p, void *const *shards, int32_t dt
 
 extern "C" int dbuf_scatter(const dbuf_plan_t *p, const void *const *src, int32_t dtype,
                             void *const *shards, void *stream) {
+    if (p && p->slice_k >= 0) return DBUF_EINVAL;  // needs every shard
     int rc = check_plan(p);
     if (rc) return rc;
     if (!dtype_ok(dtype)) return DBUF_EINVAL;

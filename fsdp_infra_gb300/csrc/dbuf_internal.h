@@ -17,10 +17,14 @@ constexpr int64_t kChunkElems = 16384;
 // Blocks per work item of the row-block (1 x qc) quantisation kernel.
 constexpr int32_t kRowItemBlocks = 64;
 
-// One tensor of the group, as the kernels see it (72 bytes).
+// One tensor of the group, as the kernels see it (80 bytes).  In a slice plan
+// (one shard of a parent plan as a rank's local buffer) a tensor is its piece
+// inside the slice: buf_off is local and src_off is the piece's first element
+// within the user tensor (0 in a full plan).
 struct TensorDesc {
     int64_t buf_off;    // l_t
     int64_t numel;      // n_t
+    int64_t src_off;    // first element of this (piece of the) tensor in the user tensor
     int64_t rows;
     int64_t cols;
     int64_t scale_off;  // first block scale of this tensor
@@ -32,7 +36,7 @@ struct TensorDesc {
     int32_t chunk_begin;
     int32_t chunk_end;
 };
-static_assert(sizeof(TensorDesc) == 72, "TensorDesc layout");
+static_assert(sizeof(TensorDesc) == 80, "TensorDesc layout");
 
 // A contiguous piece of one tensor: elements [off, off+len) of tensor `tensor`.
 struct Chunk {
@@ -168,8 +172,13 @@ int launch_unpack(const dbuf_plan_t *p, const void *buf, int buf_dt, void *const
                   void *stream);
 int launch_sac(const dbuf_plan_t *p, void *grad, int grad_dt, float *acc, float scale,
                void *stream);
+// tensor_norms and total_norm may be null; tensor_sumsq (optional) receives each
+// tensor's fp64 sum of squares.
 int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_norms,
-                float *total_norm, int32_t *nonfinite, void *workspace, void *stream);
+                float *total_norm, int32_t *nonfinite, void *workspace, void *stream,
+                double *tensor_sumsq = nullptr);
+int launch_norm_finish(const dbuf_plan_t *p, const double *sumsq, float *tensor_norms,
+                       float *total_norm, void *stream);
 int launch_quant(const dbuf_plan_t *p, const float *buf, uint8_t *codes, float *scales,
                  void *stream);
 
@@ -233,6 +242,14 @@ struct dbuf_plan {
     size_t n_opt_rest = 0;               // opt_items[0, n_opt_rest): tensors without p8 items
     std::vector<int64_t> state_offsets;  // [n], -1 for quantised tensors
     int64_t n_state = 0;
+
+    // Slice plans (dbuf_plan_slice): shard slice_k of a parent plan, whose
+    // global positions [slice_base, slice_base + total) are this plan's local
+    // positions [0, total).  slice_k = -1 for a full plan.
+    int32_t slice_k = -1;
+    int64_t slice_base = 0;
+    int64_t scale_base = 0;              // global index of the slice's first block scale
+    std::vector<int64_t> src_offsets;    // [n] piece start within each user tensor (slices)
 
     bool uploaded = false;
     dbuf::DeviceTables dev;

@@ -12,6 +12,8 @@
 // kChunkElems elements; kChunkSplit CTAs share a chunk, each handling its part
 // with 16-byte vector loads and stores (8 elements per thread per unit, kUnroll
 // units in flight per thread), and a scalar tail.  Padding between tensors is never touched.
+// In a slice plan a tensor is its piece inside one shard: the user tensor is read
+// or written from the piece's first element (src_off) on.
 #include "common.cuh"
 
 namespace dbuf {
@@ -45,8 +47,9 @@ __global__ void __launch_bounds__(kThreads)
                 const void *const *__restrict__ src, char *__restrict__ buf) {
     pdl_enter();
     const Chunk c = sub_chunk(chunks);
-    const char *s = static_cast<const char *>(src[c.tensor]) + c.off * elem_bytes<SRC>();
-    char *d = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<DST>();
+    const TensorDesc &t = td[c.tensor];
+    const char *s = static_cast<const char *>(src[c.tensor]) + (t.src_off + c.off) * elem_bytes<SRC>();
+    char *d = buf + (t.buf_off + c.off) * elem_bytes<DST>();
     copy_cast_range<SRC, DST>(s, d, c.len);
 }
 
@@ -56,8 +59,9 @@ __global__ void __launch_bounds__(kThreads)
                   const char *__restrict__ buf, void *const *__restrict__ dst) {
     pdl_enter();
     const Chunk c = sub_chunk(chunks);
-    const char *s = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<SRC>();
-    char *d = static_cast<char *>(dst[c.tensor]) + c.off * elem_bytes<DST>();
+    const TensorDesc &t = td[c.tensor];
+    const char *s = buf + (t.buf_off + c.off) * elem_bytes<SRC>();
+    char *d = static_cast<char *>(dst[c.tensor]) + (t.src_off + c.off) * elem_bytes<DST>();
     copy_cast_range<SRC, DST>(s, d, c.len);
 }
 

@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kThreads)
     norm_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td, int n,
                 uint32_t n_nonempty, const char *__restrict__ buf, NormWorkspace w,
                 float *__restrict__ tensor_norms, float *__restrict__ total_norm,
-                int32_t *__restrict__ nonfinite) {
+                int32_t *__restrict__ nonfinite, double *__restrict__ tensor_sumsq) {
     __shared__ double sh[kWarps];
     __shared__ int last;
     pdl_enter();
@@ -171,7 +171,8 @@ __global__ void __launch_bounds__(kThreads)
     if (threadIdx.x == 0) {
         w.tsum[t] = ts;
         w.tflag[t] = tf;
-        tensor_norms[t] = float(sqrt(ts));
+        if (tensor_norms) tensor_norms[t] = float(sqrt(ts));
+        if (tensor_sumsq) tensor_sumsq[t] = ts;
         __threadfence();
         last = (atomicAdd(&w.tickets[n], 1u) + 1u == n_nonempty);
         if (last) w.tickets[n] = 0u;
@@ -188,25 +189,47 @@ __global__ void __launch_bounds__(kThreads)
             tot += __ldcg(&w.tsum[i]);
             f |= __ldcg(&w.tflag[i]);
         } else {
-            tensor_norms[i] = 0.0f;
+            if (tensor_norms) tensor_norms[i] = 0.0f;
+            if (tensor_sumsq) tensor_sumsq[i] = 0.0;
         }
     }
     f = __syncthreads_or(f);
     tot = block_sum(tot, sh);
     if (threadIdx.x == 0) {
-        *total_norm = float(sqrt(tot));
+        if (total_norm) *total_norm = float(sqrt(tot));
         *nonfinite = f ? 1 : 0;
     }
 }
 
 // Outputs of a group without any element (no chunk to launch a CTA for).
 __global__ void norm_empty_kernel(int n, float *tensor_norms, float *total_norm,
-                                  int32_t *nonfinite) {
-    for (int i = threadIdx.x; i < n; i += blockDim.x) tensor_norms[i] = 0.0f;
+                                  int32_t *nonfinite, double *tensor_sumsq) {
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+        if (tensor_norms) tensor_norms[i] = 0.0f;
+        if (tensor_sumsq) tensor_sumsq[i] = 0.0;
+    }
     if (threadIdx.x == 0) {
-        *total_norm = 0.0f;
+        if (total_norm) *total_norm = 0.0f;
         *nonfinite = 0;
     }
+}
+
+// Norms from per-tensor sums of squares that were added up across shards (the
+// AllReduce of the ranks' partials): each tensor's norm, and the global norm
+// from the sums in a fixed order (strided per thread, then the CTA tree), in
+// fp64, rounded to fp32.  One CTA.
+__global__ void __launch_bounds__(kThreads)
+    norm_finish_kernel(int n, const double *__restrict__ sumsq, float *__restrict__ tensor_norms,
+                       float *__restrict__ total_norm) {
+    __shared__ double sh[kWarps];
+    double tot = 0.0;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+        const double v = sumsq[i];
+        tensor_norms[i] = float(sqrt(v));
+        tot += v;
+    }
+    tot = block_sum(tot, sh);
+    if (threadIdx.x == 0) *total_norm = float(sqrt(tot));
 }
 
 }  // namespace
@@ -226,12 +249,21 @@ size_t norm_ticket_offset(const dbuf_plan_t *p) {
 
 size_t norm_ticket_bytes(const dbuf_plan_t *p) { return sizeof(uint32_t) * (size_t(p->n) + 1); }
 
+int launch_norm_finish(const dbuf_plan_t *p, const double *sumsq, float *tensor_norms,
+                       float *total_norm, void *stream) {
+    norm_finish_kernel<<<1, kThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+        p->n, sumsq, tensor_norms, total_norm);
+    return cudaGetLastError();
+}
+
 int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_norms,
-                float *total_norm, int32_t *nonfinite, void *workspace, void *stream) {
+                float *total_norm, int32_t *nonfinite, void *workspace, void *stream,
+                double *tensor_sumsq) {
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const unsigned nc = unsigned(p->chunks.size());
     if (nc == 0) {
-        norm_empty_kernel<<<1, 256, 0, st>>>(p->n, tensor_norms, total_norm, nonfinite);
+        norm_empty_kernel<<<1, 256, 0, st>>>(p->n, tensor_norms, total_norm, nonfinite,
+                                             tensor_sumsq);
         return cudaGetLastError();
     }
     NormWorkspace w = carve(p, workspace);
@@ -242,9 +274,9 @@ int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_nor
     const char *b = static_cast<const char *>(buf);
     if (dt == DBUF_F32)
         return launch_pdl(norm_kernel<DBUF_F32>, nc, kThreads, 0, st, chunks, td, p->n, nonempty, b,
-                          w, tensor_norms, total_norm, nonfinite);
+                          w, tensor_norms, total_norm, nonfinite, tensor_sumsq);
     return launch_pdl(norm_kernel<DBUF_BF16>, nc, kThreads, 0, st, chunks, td, p->n, nonempty, b, w,
-                      tensor_norms, total_norm, nonfinite);
+                      tensor_norms, total_norm, nonfinite, tensor_sumsq);
 }
 
 }  // namespace dbuf

@@ -241,6 +241,7 @@ void build_tables(dbuf_plan_t *p) {
         const dbuf_tensor_spec &s = p->specs[t];
         TensorDesc &d = p->tdesc[t];
         d.buf_off = p->offsets[t];
+        d.src_off = p->src_offsets.empty() ? 0 : p->src_offsets[t];
         d.rows = s.rows;
         d.cols = s.cols;
         d.numel = s.rows * s.cols;
@@ -443,6 +444,102 @@ extern "C" int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
         return DBUF_ENOMEM;
     }
     *out = p;
+    return DBUF_OK;
+}
+
+extern "C" int dbuf_plan_slice(const dbuf_plan_t *p, int32_t k, dbuf_plan_t **out) {
+    if (!out) return DBUF_EINVAL;
+    *out = nullptr;
+    if (!p || p->slice_k >= 0 || k < 0 || k >= p->m) return DBUF_EINVAL;
+    dbuf_plan_t *s = new (std::nothrow) dbuf_plan_t();
+    if (!s) return DBUF_ENOMEM;
+    try {
+        const int32_t n = p->n;
+        const int64_t B0 = p->bounds[k], B1 = p->bounds[k + 1], len = B1 - B0;
+        s->n = n;
+        s->m = 1;
+        s->align = p->align;
+        s->even = true;
+        s->units.assign(1, 1);
+        s->S = len;
+        s->total = len;
+        s->bounds = {0, len};
+        s->slice_k = k;
+        s->slice_base = B0;
+        s->specs.resize(n);
+        s->offsets.assign(n, 0);
+        s->src_offsets.assign(n, 0);
+        int64_t scale_base = 0;
+        for (int32_t t = 0; t < n; ++t) {
+            const dbuf_tensor_spec &ps = p->specs[t];
+            const int64_t l = p->offsets[t], nt = ps.rows * ps.cols;
+            const int64_t lo = std::max(l, B0), hi = std::min(l + nt, B1);
+            dbuf_tensor_spec ss = ps;
+            ss.gran_rows = 0;
+            if (hi > lo) {
+                const int64_t e0 = lo - l, pl = hi - lo;
+                s->offsets[t] = lo - B0;
+                s->src_offsets[t] = e0;
+                if (ps.quant != DBUF_QUANT_NONE) {
+                    // shard cuts fall on whole units, and a quantised tensor's unit is a
+                    // whole number of block rows: the piece is rows [r0, r0 + pr)
+                    const int64_t qr =
+                        ps.qblock_rows > 0 ? ps.qblock_rows : std::max<int64_t>(ps.rows, 1);
+                    const int64_t blk_row = qr * ps.cols;
+                    if (e0 % blk_row != 0 || (hi != l + nt && pl % blk_row != 0)) {
+                        delete s;
+                        return DBUF_EINVAL;
+                    }
+                    ss.rows = pl / ps.cols;
+                    ss.qblock_rows = int32_t(qr);
+                } else {
+                    ss.rows = pl;
+                    ss.cols = 1;
+                }
+            } else {
+                s->offsets[t] = std::min(std::max<int64_t>(l - B0, 0), len);
+                s->src_offsets[t] = l + nt <= B0 ? nt : 0;
+                ss.rows = 0;
+                if (ps.quant == DBUF_QUANT_NONE) ss.cols = 1;
+            }
+            s->specs[t] = ss;
+            // global block scales that lie before the slice
+            if (ps.quant != DBUF_QUANT_NONE && nt > 0) {
+                const int64_t qr =
+                    ps.qblock_rows > 0 ? ps.qblock_rows : std::max<int64_t>(ps.rows, 1);
+                const int64_t qc =
+                    ps.qblock_cols > 0 ? ps.qblock_cols : std::max<int64_t>(ps.cols, 1);
+                const int64_t nbc = (ps.cols + qc - 1) / qc, nbr = (ps.rows + qr - 1) / qr;
+                if (l + nt <= B0) scale_base += nbr * nbc;
+                else if (l < B0) scale_base += (B0 - l) / (qr * ps.cols) * nbc;
+            }
+        }
+        s->scale_base = scale_base;
+        build_tables(s);
+        if (s->chunks.size() > size_t(INT32_MAX) || s->pieces.size() > size_t(INT32_MAX) ||
+            s->pipe_items.size() > size_t(INT32_MAX) || s->p8_items.size() > size_t(INT32_MAX) ||
+            s->opt_items.size() + s->opt_plain.size() > size_t(INT32_MAX)) {
+            delete s;
+            return DBUF_ERANGE;
+        }
+    } catch (const std::bad_alloc &) {
+        delete s;
+        return DBUF_ENOMEM;
+    }
+    *out = s;
+    return DBUF_OK;
+}
+
+extern "C" int dbuf_plan_slice_info(const dbuf_plan_t *s, int32_t *k, int64_t *global_offset,
+                                    int64_t *src_offsets, int64_t *numels, int64_t *scale_base) {
+    if (!s || s->slice_k < 0) return DBUF_EINVAL;
+    if (k) *k = s->slice_k;
+    if (global_offset) *global_offset = s->slice_base;
+    for (int32_t t = 0; t < s->n; ++t) {
+        if (src_offsets) src_offsets[t] = s->src_offsets[t];
+        if (numels) numels[t] = s->tdesc[t].numel;
+    }
+    if (scale_base) *scale_base = s->scale_base;
     return DBUF_OK;
 }
 

@@ -46,7 +46,8 @@ EXPORTS = ("dbuf_plan", "dbuf_plan_query", "dbuf_plan_upload", "dbuf_plan_free",
            "dbuf_norm_nonfinite", "dbuf_norm_nonfinite_noalloc", "dbuf_block_quant",
            "dbuf_device_status", "dbuf_adamw_step", "dbuf_plan_state_offsets",
            "dbuf_adamw8_step", "dbuf_order", "dbuf_gather", "dbuf_scatter",
-           "dbuf_selftest_wait_timeout", "dbuf_strerror", "dbuf_last_cuda_error")
+           "dbuf_selftest_wait_timeout", "dbuf_strerror", "dbuf_last_cuda_error",
+           "dbuf_plan_slice", "dbuf_plan_slice_info", "dbuf_norm_sumsq", "dbuf_norm_finish")
 
 # Bytes of the library's static scratch used by dbuf_norm_nonfinite_noalloc.
 DBUF_NOALLOC_SCRATCH_BYTES = 1 << 20
@@ -110,6 +111,14 @@ def _lib_handle():
         L.dbuf_norm_nonfinite.restype = ctypes.c_int
         L.dbuf_norm_nonfinite_noalloc.argtypes = [P, P, i32, P, P, P, P]
         L.dbuf_norm_nonfinite_noalloc.restype = ctypes.c_int
+        L.dbuf_plan_slice.argtypes = [P, i32, ctypes.POINTER(ctypes.c_void_p)]
+        L.dbuf_plan_slice.restype = ctypes.c_int
+        L.dbuf_plan_slice_info.argtypes = [P, P, P, P, P, P]
+        L.dbuf_plan_slice_info.restype = ctypes.c_int
+        L.dbuf_norm_sumsq.argtypes = [P, P, i32, P, P, P, ctypes.c_size_t, P]
+        L.dbuf_norm_sumsq.restype = ctypes.c_int
+        L.dbuf_norm_finish.argtypes = [P, P, P, P, P]
+        L.dbuf_norm_finish.restype = ctypes.c_int
         L.dbuf_block_quant.argtypes = [P, P, P, P, P]
         L.dbuf_block_quant.restype = ctypes.c_int
         L.dbuf_adamw_step.argtypes = [P, P, P, P, P, P, P, P, P]
@@ -191,6 +200,35 @@ def dbuf_plan_query(plan: int, n: int, m: int) -> dict:
                                          soff, ctypes.byref(ns)), "dbuf_plan_query")
     return {"S": S.value, "total": total.value, "offsets": list(off)[:n],
             "shard_bounds": list(bounds), "scale_offsets": list(soff)[:n], "n_scales": ns.value}
+
+
+def dbuf_plan_slice(plan: int, k: int) -> int:
+    """The plan of shard slice k as a rank's local buffer (a new plan handle)."""
+    out = ctypes.c_void_p()
+    _check(_lib_handle().dbuf_plan_slice(plan, k, ctypes.byref(out)), "dbuf_plan_slice")
+    return out.value
+
+
+def dbuf_plan_slice_info(slice_plan: int, n: int) -> dict:
+    k, off, base = ctypes.c_int32(), ctypes.c_int64(), ctypes.c_int64()
+    src = (ctypes.c_int64 * max(n, 1))()
+    num = (ctypes.c_int64 * max(n, 1))()
+    _check(_lib_handle().dbuf_plan_slice_info(slice_plan, ctypes.byref(k), ctypes.byref(off), src,
+                                              num, ctypes.byref(base)), "dbuf_plan_slice_info")
+    return {"k": k.value, "global_offset": off.value, "src_offsets": list(src)[:n],
+            "numels": list(num)[:n], "scale_base": base.value}
+
+
+def dbuf_norm_sumsq(plan: int, buf: int, dtype: int, tensor_sumsq: int, nonfinite: int,
+                    workspace: int, workspace_bytes: int, stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_norm_sumsq(plan, buf, dtype, tensor_sumsq, nonfinite, workspace,
+                                         workspace_bytes, stream), "dbuf_norm_sumsq")
+
+
+def dbuf_norm_finish(plan: int, tensor_sumsq: int, tensor_norms: int, total_norm: int,
+                     stream: int = 0) -> None:
+    _check(_lib_handle().dbuf_norm_finish(plan, tensor_sumsq, tensor_norms, total_norm, stream),
+           "dbuf_norm_finish")
 
 
 def dbuf_plan_upload(plan: int, stream: int = 0) -> None:

@@ -33,9 +33,13 @@ class DBuffer:
                  align_elems: int = 16, device: Optional[torch.device] = None):
         self.specs = list(specs)
         self.n = len(self.specs)
-        self.m = m
         self.local_units = list(local_units) if local_units is not None else None
-        self.handle = _c.dbuf_plan(self.specs, m, local_units, align_elems)
+        self._setup(_c.dbuf_plan(self.specs, m, local_units, align_elems), m, device)
+        self.slice_k = None
+
+    def _setup(self, handle: int, m: int, device) -> None:
+        self.m = m
+        self.handle = handle
         q = _c.dbuf_plan_query(self.handle, self.n, m)
         self.S: int = q["S"]
         self.total: int = q["total"]
@@ -53,6 +57,24 @@ class DBuffer:
         self._ptr_tables: Dict[Tuple[int, ...], torch.Tensor] = {}
         self._workspace: Optional[torch.Tensor] = None
         self.uploaded = False
+
+    def slice(self, k: int) -> "DBuffer":
+        """Shard slice k as a rank's local DBuffer (not yet uploaded): its buffers
+        hold the B_{k+1} - B_k elements of [B_k, B_{k+1}); the group operators run
+        on the tensors' pieces inside the slice and take the same whole user
+        tensors as this DBuffer."""
+        sl = DBuffer.__new__(DBuffer)
+        sl.specs = self.specs
+        sl.n = self.n
+        sl.local_units = None
+        sl._setup(_c.dbuf_plan_slice(self.handle, k), 1, self.device)
+        info = _c.dbuf_plan_slice_info(sl.handle, sl.n)
+        sl.slice_k = info["k"]
+        sl.global_offset = info["global_offset"]
+        sl.src_offsets = info["src_offsets"]
+        sl.piece_numels = info["numels"]
+        sl.scale_base = info["scale_base"]
+        return sl
 
     # -- lifetime ------------------------------------------------------------
     def upload(self, stream: Optional[torch.cuda.Stream] = None) -> "DBuffer":
@@ -180,6 +202,33 @@ class DBuffer:
                                norms.data_ptr(), total.data_ptr(), flag.data_ptr(),
                                ws.data_ptr(), ws.numel(), self._stream(stream))
         return norms[:self.n], total, flag
+
+    def norm_sumsq(self, buf: torch.Tensor, out: Optional[Tuple] = None, stream=None,
+                   workspace: Optional[torch.Tensor] = None):
+        """Per-tensor fp64 sums of squares and the non-finite flag (device tensors
+        sumsq[n] f64, nonfinite[1] i32): the partials a sharded norm adds up."""
+        self._check_buf(buf)
+        if out is None:
+            out = (torch.empty(max(self.n, 1), dtype=torch.float64, device=self.device),
+                   torch.empty(1, dtype=torch.int32, device=self.device))
+        sumsq, flag = out
+        ws = self.workspace() if workspace is None else workspace
+        _c.dbuf_norm_sumsq(self.handle, buf.data_ptr(), dtype_code(buf.dtype), sumsq.data_ptr(),
+                           flag.data_ptr(), ws.data_ptr(), ws.numel(), self._stream(stream))
+        return sumsq[:self.n], flag
+
+    def norm_finish(self, sumsq: torch.Tensor, out: Optional[Tuple] = None, stream=None):
+        """Norms from (all-reduced) per-tensor sums of squares: (tensor_norms[n]
+        f32, total_norm[1] f32) device tensors."""
+        if sumsq.dtype != torch.float64 or sumsq.numel() < self.n or sumsq.device != self.device:
+            raise ValueError("sumsq must be a float64 device tensor of n elements")
+        if out is None:
+            out = (torch.empty(max(self.n, 1), dtype=torch.float32, device=self.device),
+                   torch.empty(1, dtype=torch.float32, device=self.device))
+        norms, total = out
+        _c.dbuf_norm_finish(self.handle, sumsq.data_ptr(), norms.data_ptr(), total.data_ptr(),
+                            self._stream(stream))
+        return norms[:self.n], total
 
     def block_quant(self, buf: torch.Tensor, codes: Optional[torch.Tensor] = None,
                     scales: Optional[torch.Tensor] = None, stream=None):

@@ -165,6 +165,48 @@ int dbuf_plan_query(const dbuf_plan_t *plan, int64_t *S, int64_t *total, int64_t
                     int64_t *shard_bounds, int64_t *scale_offsets, int64_t *n_scales);
 
 /*
+ * dbuf_plan_slice -- host only, no CUDA call.  The plan of one shard slice as a
+ * rank's local buffer: shard k of `plan` ([B_k, B_{k+1}) of the flat buffer)
+ * becomes a plan of its own whose buffer is the rank's local slice, local
+ * position 0 = global position B_k, `total` = B_{k+1} - B_k.  [veScale-FSDP §5
+ * DBuffer: each rank owns one slice of the global buffer, and AllGather /
+ * ReduceScatter move whole slices in place; §4 and §6.3: no block crosses a
+ * shard, so the group operators run on a slice without communication.]
+ * Every operator of this header except dbuf_gather / dbuf_scatter runs on a
+ * slice plan exactly as on a full plan, over the pieces of the tensors that lie
+ * inside the slice, and its result on the local buffer equals the full plan's
+ * result on [B_k, B_{k+1}); nothing outside the slice is read or written.
+ * Tensors keep their indices 0..n-1 (a tensor outside the slice is an empty
+ * piece):
+ *   - pack / unpack take the same device array of n pointers to the WHOLE user
+ *     tensors as the full plan, and read or write only each tensor's piece,
+ *     from its first element src_offsets[t] (dbuf_plan_slice_info) on;
+ *   - dbuf_plan_query on a slice plan gives local offsets, S = total = the
+ *     slice length, shard bounds {0, total}, and a local numbering of the
+ *     slice's block scales (scale_offsets, n_scales): they are the contiguous
+ *     range [scale_base, scale_base + n_scales) of the full plan's scales;
+ *   - norms are those of the pieces (dbuf_norm_sumsq gives their fp64 sums of
+ *     squares for an AllReduce across slices);
+ *   - the 8-bit AdamW state of a slice is the slice's own (codes in the local
+ *     layout, local scales, compact fp32 moments of its unquantised pieces).
+ * A slice plan is uploaded and freed like any plan and is independent of its
+ * parent afterwards.  Errors: DBUF_EINVAL (plan NULL or itself a slice, k out
+ * of [0, m)), DBUF_ERANGE, DBUF_ENOMEM.
+ */
+int dbuf_plan_slice(const dbuf_plan_t *plan, int32_t k, dbuf_plan_t **out);
+
+/*
+ * dbuf_plan_slice_info -- host only.  For a slice plan: *k its shard index,
+ * *global_offset = B_k, src_offsets[n] each tensor's first element inside the
+ * slice (the piece starts there in the user tensor; for a tensor wholly outside
+ * the slice 0 or n_t), numels[n] each piece's element count (0 outside),
+ * *scale_base the full plan's index of the slice's first block scale.  Any
+ * output may be NULL.  Errors: DBUF_EINVAL (NULL, or not a slice plan).
+ */
+int dbuf_plan_slice_info(const dbuf_plan_t *slice, int32_t *k, int64_t *global_offset,
+                         int64_t *src_offsets, int64_t *numels, int64_t *scale_base);
+
+/*
  * dbuf_plan_upload -- copies the plan's descriptor tables (tensor table, chunk
  * table, quantisation work lists) to the current device: the persistent
  * address mapping of [veScale-FSDP §5 DBuffer, zero-copy access].  Allocates
@@ -251,6 +293,31 @@ size_t dbuf_workspace_bytes(const dbuf_plan_t *plan, int32_t op);
 int dbuf_norm_nonfinite(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
                         float *tensor_norms, float *total_norm, int32_t *nonfinite,
                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * dbuf_norm_sumsq -- the first half of a sharded norm: for each tensor (of a
+ * slice plan: each piece) the sum of squares of its elements in fp64, and the
+ * non-finite flag, in the same single launch and fixed order as
+ * dbuf_norm_nonfinite (which takes the square roots).  The per-tensor sums of
+ * the m slices are then added by the caller's AllReduce and turned into norms
+ * by dbuf_norm_finish.  [veScale OpDispatcher: the ragged norm handler when
+ * shard and tensor boundaries differ; PyTorch FSDP known limitations: a
+ * per-parameter norm needs the partial sums of every shard.]
+ * tensor_sumsq: device double[n]; nonfinite: device int32 (0 or 1); workspace
+ * as for dbuf_norm_nonfinite.  Errors as for dbuf_norm_nonfinite.
+ */
+int dbuf_norm_sumsq(const dbuf_plan_t *plan, const void *buf, int32_t dtype, double *tensor_sumsq,
+                    int32_t *nonfinite, void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * dbuf_norm_finish -- the second half: tensor_norms[t] = sqrt(tensor_sumsq[t])
+ * and total_norm = sqrt of the sum over t (added in a fixed order), in fp64,
+ * rounded to fp32.  One small launch.  Inputs and outputs are device pointers
+ * (double[n]; float[n], float).  The plan (full or slice) gives n.
+ * Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
+ */
+int dbuf_norm_finish(const dbuf_plan_t *plan, const double *tensor_sumsq, float *tensor_norms,
+                     float *total_norm, void *stream);
 
 /*
  * dbuf_block_quant -- block-wise absmax quantisation of an fp32 buffer, blocks
@@ -420,8 +487,8 @@ int dbuf_adamw8_step(const dbuf_plan_t *plan, float *params, const float *grads,
  *   dst:    device array of n device pointers; dst[t] receives the numel_t
  *           elements of tensor t; a NULL entry skips the tensor.
  * Padding bytes of the shards are never read.  16-byte aligned ends take the
- * vector path.  Errors: DBUF_EINVAL, DBUF_ENOTUPLOADED, DBUF_EDEVICE,
- * DBUF_ECUDA.
+ * vector path.  Errors: DBUF_EINVAL (also for a slice plan: the gather needs
+ * every shard), DBUF_ENOTUPLOADED, DBUF_EDEVICE, DBUF_ECUDA.
  */
 int dbuf_gather(const dbuf_plan_t *plan, void *const *shards, int32_t dtype, void *const *dst,
                 void *stream);

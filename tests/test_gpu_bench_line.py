@@ -55,3 +55,20 @@ def test_bench_line_fields(dbuf_lib, oracle_lib):
         assert clocks["reasons"]
     for op in ("pack_cast", "unpack", "scale_accum_zero", "norm_nonfinite", "block_quant"):
         assert d["ops"][op]["gbs"] > 0
+
+
+@pytest.mark.gpu
+def test_bench_exchange_mode_on_one_gpu(dbuf_lib):
+    """--exchange runs the sharded step (ShardedStep around NCCL collectives) with
+    m = the number of GPUs; on one GPU the process group has one rank, which
+    exercises the whole code path (plans, slice plans, collectives, operators)."""
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--exchange",
+                        "--workload", "tiny", "--steps", "2", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-3000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.strip().startswith("{")]
+    assert len(lines) == 1, r.stdout[-3000:]
+    d = json.loads(lines[0])
+    assert d["mode"] == "exchange" and d["n_gpus"] == 1 and d["config"]["m"] == 1
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    assert d["collective_bytes_per_rank"] > 0 and d["op_bytes_per_rank"] > 0
