@@ -704,6 +704,8 @@ def run_ours(args):
     # ---- the next row: fused AdamW step over every DBuffer (separate timing)
     adamw = None if args.no_adamw else run_adamw(stack, args, world, peak, barrier)
     adamw8 = None if args.no_adamw else run_adamw8(stack, args, world, peak, barrier)
+    adamw8_128 = (None if args.no_adamw else
+                  run_adamw8(stack, args, world, peak, barrier, block=(128, 128)))
     gather = None if args.no_adamw else run_gather(stack, args, world, peak, barrier)
 
     # ---- end to end: host inputs (pinned) -> device, operators, results -> host
@@ -736,8 +738,8 @@ def run_ours(args):
                 "frac_of_nominal_8tbs": round(value / world / NOMINAL_HBM_GBS, 4),
                 "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
                 "gpu_launches": stack.launches_per_step * args.steps,
-                "next_rows": ({"adamw": adamw, "adamw8": adamw8, "gather_scatter": gather}
-                              if adamw else None),
+                "next_rows": ({"adamw": adamw, "adamw8": adamw8, "adamw8_128x128": adamw8_128,
+                               "gather_scatter": gather} if adamw else None),
                 "launch": "eager" if args.eager else "cuda_graph (K steps captured once, replayed)",
                 "ops_note": ("per operator, outside the timed region: its launches over every "
                              "DBuffer back to back, timed over 3 passes" +
@@ -921,10 +923,11 @@ def run_adamw(stack, args, world, peak, barrier):
             "algorithmic_layer_launch": 28 * stack.w.groups[0].numel}
 
 
-def run_adamw8(stack, args, world, peak, barrier):
+def run_adamw8(stack, args, world, peak, barrier, block=(32, 32)):
     """8-bit AdamW (dbuf_adamw8_step) over every DBuffer of the workload, each
-    group re-planned as the 8-bit Adam experiment shards it (32x32 INT8 blocks,
-    32-row granularity for matrices): fp32 master parameters and gradients,
+    group re-planned as the 8-bit Adam experiment shards it (block x block INT8
+    blocks at block-row granularity for matrices; 32x32 in the experiment,
+    128x128 the big-block kernel's case): fp32 master parameters and gradients,
     8-bit block moments, compact fp32 moments for vectors; clipped to max_norm
     1.0 with the group's device norm.  One plan and one set of buffers per group
     kind, stepped once per DBuffer (the buffers exceed L2).  K steps captured
@@ -939,7 +942,7 @@ def run_adamw8(stack, args, world, peak, barrier):
     w = stack.w
     kinds = {}
     for gi, g in enumerate(w.groups):
-        g8 = adam8_group(g)
+        g8 = adam8_group(g, block)
         db = DBuffer(g8.tensors, w.m, None, w.align, device=device).upload()
         p32 = torch.zeros(db.total, dtype=torch.float32, device=device)
         g32 = torch.zeros(db.total, dtype=torch.float32, device=device)
@@ -950,8 +953,9 @@ def run_adamw8(stack, args, world, peak, barrier):
         out = db.norm_nonfinite(g32)
         qe = sum(spec.numel for spec in g8.tensors if spec.quant)
         pe = sum(spec.numel for spec in g8.tensors if not spec.quant)
-        # launches: the pipelined kernel once per 16 quantised tensors (the tensor
-        # maps one launch carries), the register kernel once for the rest
+        # launches: the pipelined kernel (the stage kernel, or the big-block kernel
+        # for blocks of two stages) once per 16 quantised tensors (the tensor maps
+        # one launch carries), the register kernel once for the rest
         nq = sum(1 for spec in g8.tensors if spec.quant and spec.numel)
         rest = any(spec.numel and not spec.quant for spec in g8.tensors)
         kinds[gi] = {"db": db, "p": p32, "g": g32, "state": db.new_adamw8_state(), "out": out,
@@ -991,7 +995,8 @@ def run_adamw8(stack, args, world, peak, barrier):
     nbytes = sum(kinds[gi]["bytes"] for gi in order)
     gbs = job_throughput(nbytes, ms, world)
     elems = sum(kinds[gi]["db"].total for gi in order)
-    blk = sorted({spec.qblock for g in w.groups for spec in adam8_group(g).tensors if spec.quant})
+    blk = sorted({spec.qblock for g in w.groups for spec in adam8_group(g, block).tensors
+                  if spec.quant})
     return {"op": "dbuf_adamw8_step (fp32 params/grads, 8-bit block moments, clip to the "
                   "group's device norm)",
             "blocks": [list(b) for b in blk], "gbs": round(gbs, 1), "ms_per_step": round(ms, 4),

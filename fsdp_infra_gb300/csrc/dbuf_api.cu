@@ -55,7 +55,8 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     const size_t b_a = align256(sizeof(int32_t) * p->opt_plain.size());
     const size_t b_g = align256(sizeof(dbuf::Piece) * p->pieces.size());
     const size_t b_8 = align256(sizeof(dbuf::P8Item) * p->p8_items.size());
-    const size_t bytes = b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g + b_8 + 256;
+    const size_t b_b = align256(sizeof(dbuf::P8Item) * p->big_items.size());
+    const size_t bytes = b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g + b_8 + b_b + 256;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -82,8 +83,10 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
     t.opt_plain = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o);
     t.pieces = reinterpret_cast<dbuf::Piece *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a);
     t.p8_items = reinterpret_cast<dbuf::P8Item *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g);
-    t.status =
-        reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g + b_8);
+    t.big_items =
+        reinterpret_cast<dbuf::P8Item *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g + b_8);
+    t.status = reinterpret_cast<int32_t *>(c + b_t + b_c + b_r + b_q + b_p + b_o + b_a + b_g + b_8 +
+                                           b_b);
     t.num_sms = sms;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     e = cudaMemsetAsync(t.status, 0, sizeof(int32_t), st);
@@ -95,7 +98,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
         void *dst;
         const void *src;
         size_t n;
-    } pieces[9] = {
+    } pieces[10] = {
         {t.tensors, p->tdesc.data(), sizeof(dbuf::TensorDesc) * p->tdesc.size()},
         {t.chunks, p->chunks.data(), sizeof(dbuf::Chunk) * p->chunks.size()},
         {t.row_items, p->row_items.data(), sizeof(dbuf::RowItem) * p->row_items.size()},
@@ -105,6 +108,7 @@ extern "C" int dbuf_plan_upload(dbuf_plan_t *p, void *stream) {
         {t.opt_plain, p->opt_plain.data(), sizeof(int32_t) * p->opt_plain.size()},
         {t.pieces, p->pieces.data(), sizeof(dbuf::Piece) * p->pieces.size()},
         {t.p8_items, p->p8_items.data(), sizeof(dbuf::P8Item) * p->p8_items.size()},
+        {t.big_items, p->big_items.data(), sizeof(dbuf::P8Item) * p->big_items.size()},
     };
     for (const Piece &pc : pieces) {
         if (!pc.n) continue;

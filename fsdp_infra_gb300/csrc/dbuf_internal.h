@@ -126,6 +126,10 @@ constexpr int kOptUnitsPerLane = 2;
 // Target elements per 8-bit optimizer work item.
 constexpr int64_t kOptItemElems = 16384;
 
+// Blocks of exactly this many elements (128 x 128, 64 x 256, 256 x 64), twice a
+// stage of the pipelined 8-bit optimizer, take their own pipelined kernel.
+constexpr int64_t kBigBlockElems = 16384;
+
 constexpr int kPipeMaxRows = 128;
 constexpr int kPipeMaxCols = 128;
 constexpr int kPipeMaxTensors = 32;  // tensor maps passed per launch; more tensors take more launches
@@ -157,6 +161,7 @@ struct DeviceTables {
     int32_t *opt_plain = nullptr;    // 8-bit optimizer: chunks of the other tensors
     Piece *pieces = nullptr;         // gather / scatter: chunks split at shard bounds
     P8Item *p8_items = nullptr;      // pipelined 8-bit optimizer stages
+    P8Item *big_items = nullptr;     // pipelined 8-bit optimizer, one block of kBigBlockElems each
     int32_t *status = nullptr;       // device status word (0, or DBUF_ETIMEOUT)
     void *base = nullptr;
     size_t bytes = 0;
@@ -239,7 +244,10 @@ struct dbuf_plan {
     std::vector<dbuf::P8Item> p8_items;
     std::vector<int32_t> p8_tensors;     // slot -> tensor id
     std::vector<size_t> p8_item_start;   // [slots + 1]: first p8 item of each slot
-    size_t n_opt_rest = 0;               // opt_items[0, n_opt_rest): tensors without p8 items
+    std::vector<dbuf::P8Item> big_items;   // one item per kBigBlockElems block (slot, tensor, bi, bj)
+    std::vector<int32_t> big_tensors;      // slot -> tensor
+    std::vector<size_t> big_item_start;    // [slots + 1]
+    size_t n_opt_rest = 0;               // opt_items[0, n_opt_rest): tensors without pipelined items
     std::vector<int64_t> state_offsets;  // [n], -1 for quantised tensors
     int64_t n_state = 0;
 

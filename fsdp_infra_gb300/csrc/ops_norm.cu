@@ -5,22 +5,39 @@
 // Fully Sharded Data Parallel", sharded gradient scaler and known limitations
 // (per-parameter norms need tensor boundaries, not shard boundaries).
 //
-// One launch, deterministic (no floating-point atomics), two-level tree:
+// One launch, deterministic (the same inputs give the same bits, whatever order
+// the CTAs run in), no floating-point atomics:
 //  1. one CTA per chunk: each thread sums squares of its elements in kUnroll
-//     independent fp32 accumulators (16 terms each for a full chunk), adds
-//     them and the warp adds its 32 lanes in a fixed fp32 shuffle tree (at most
-//     about 22 roundings of 2^-24 on any chunk, far inside the 1e-5 tolerance);
-//     the 8 warp sums are combined in fp64 in a fixed order, giving one fp64
-//     partial and one non-finite flag per chunk in the workspace.  Keeping the
-//     lane-level tree in fp32 matters on this GPU, whose fp64 pipe is narrow;
-//  2. the last CTA to finish a tensor (an integer ticket per tensor) adds that
-//     tensor's chunk partials in a fixed strided order and tree, writes the
-//     tensor's norm, and takes a ticket on a global counter; the last tensor
-//     finisher adds the per-tensor sums in a fixed order and writes the global
-//     norm and flag.  The sums never depend on which CTA finishes last.
-// Square roots in fp64, results rounded to fp32.  The tickets start at zero
-// (a zero-filled workspace) and each is returned to zero by its last user, so
-// every call leaves them as it found them and needs no clearing launch.
+//     independent fp32 accumulators (16 terms each for a full chunk), the warp
+//     adds its 32 lanes in a fixed fp32 shuffle tree (at most about 22 roundings
+//     of 2^-24 on any chunk, far inside the 1e-5 tolerance), and the 8 warp sums
+//     are combined in fp64 in a fixed order: one fp64 partial per chunk, a fixed
+//     function of the chunk's values.  Keeping the lane-level tree in fp32
+//     matters on this GPU, whose fp64 pipe is narrow;
+//  2. the partial is added to its tensor's exact accumulator: a fixed-point
+//     number of kDigits 32-bit digits, digit i of weight 2^(32 i + kDigitBase),
+//     each digit held in a 64-bit counter.  The partial's 53-bit significand
+//     goes into two or three counters by integer reductions, which are exact
+//     and commutative, so a tensor's sum does not depend on the order in which
+//     its chunks finish.  A partial is an fp64 sum of eight fp32 values: it lies
+//     in [2^-149, 2^131) with its lowest bit at weight >= 2^-201, inside the
+//     digits; the top digits take the carries of up to 2^31 partials.  A chunk
+//     holding an inf or NaN adds nothing and raises the flag; a partial that
+//     overflowed fp32 sets the tensor's infinity mark;
+//  3. a tensor's sum: its carries resolved, the exact sum rounded once to fp64
+//     (round to nearest even: tensor_sumsq), the square root in fp64 rounded to
+//     fp32 (tensor_norms).  Groups of up to kOneFinisher tensors: each CTA takes
+//     one acquire-release ticket on a global counter, and the launch's last CTA
+//     finishes every tensor (one load and one store of 128 bytes each), so the
+//     chain at the end of the launch is one ticket round trip and that pass.
+//     Larger groups (many small tensors): each CTA takes a ticket on its
+//     tensor's counter, the tensor's last CTA finishes that tensor and takes a
+//     ticket on the global counter, so the per-tensor work is spread over the
+//     launch.  Either way the last CTA adds the per-tensor fp64 sums in the same
+//     fixed order (strided per thread, then the CTA tree) for the global norm,
+//     writes the flag, and returns every counter to zero, so each call leaves
+//     the workspace as it found it and needs no clearing launch; both ways give
+//     the same bits.
 #include "common.cuh"
 
 namespace dbuf {
@@ -28,31 +45,108 @@ namespace {
 
 constexpr int kUnroll = 4;
 constexpr int kWarps = kThreads / 32;
+constexpr int kDigits = 16;        // 32-bit digits of a tensor's exact accumulator
+constexpr int kDigitBase = -224;   // weight of digit 0 is 2^kDigitBase
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// Groups of at most this many tensors finish in the launch's last CTA; larger
+// groups finish each tensor in the CTA that completes it (see step 3 above).
+constexpr int kOneFinisher = 256;
+
 struct NormWorkspace {
-    double *partial;    // [nc]
-    int32_t *flags;     // [nc]
-    double *tsum;       // [n]
-    int32_t *tflag;     // [n]
-    uint32_t *tickets;  // [n + 1]: per-tensor tickets, then the global one
+    unsigned long long *acc;  // [n][kDigits] digit counters of each tensor's sum of squares
+    double *tsum;             // [n] each tensor's sum (per-tensor finishing)
+    uint32_t *tticket;        // [n] chunks finished per tensor (per-tensor finishing)
+    uint32_t *ticket;         // [0] CTAs (or tensors) finished, [1] non-finite flag
 };
 
 NormWorkspace carve(const dbuf_plan_t *p, void *ws) {
     char *b = static_cast<char *>(ws);
-    const size_t nc = p->chunks.size(), n = size_t(p->n);
+    const size_t n = size_t(p->n);
     NormWorkspace w;
-    w.partial = reinterpret_cast<double *>(b);
-    b += align256(sizeof(double) * nc);
-    w.flags = reinterpret_cast<int32_t *>(b);
-    b += align256(sizeof(int32_t) * nc);
+    w.acc = reinterpret_cast<unsigned long long *>(b);
+    b += align256(sizeof(unsigned long long) * kDigits * n);
     w.tsum = reinterpret_cast<double *>(b);
     b += align256(sizeof(double) * n);
-    w.tflag = reinterpret_cast<int32_t *>(b);
-    b += align256(sizeof(int32_t) * n);
-    w.tickets = reinterpret_cast<uint32_t *>(b);
+    w.tticket = reinterpret_cast<uint32_t *>(b);
+    b += align256(sizeof(uint32_t) * n);
+    w.ticket = reinterpret_cast<uint32_t *>(b);
     return w;
+}
+
+
+// Exact addition of a finite partial s in [2^-149, 2^131) to a tensor's digit
+// counters: its significand m (53 bits) times 2^(e - 52) sits at bit position
+// sh = e - 52 - kDigitBase >= 23 of the fixed-point number.
+__device__ __forceinline__ void add_exact(unsigned long long *acc, double s) {
+    const unsigned long long bits = static_cast<unsigned long long>(__double_as_longlong(s));
+    const int ex = int((bits >> 52) & 0x7ffu);
+    const unsigned long long m = (bits & ((1ull << 52) - 1)) | (1ull << 52);
+    const int sh = ex - 1075 - kDigitBase;
+    const int d = sh >> 5, r = sh & 31;
+    const unsigned long long lo = m << r;
+    atomicAdd(&acc[d], lo & 0xffffffffull);
+    atomicAdd(&acc[d + 1], lo >> 32);
+    if (r > 11) atomicAdd(&acc[d + 2], m >> (64 - r));
+}
+
+// The exact sum held in a tensor's digit counters, rounded once to fp64 (round
+// to nearest, ties to even); +inf when the infinity mark is set.
+__device__ __forceinline__ double exact_sum(const unsigned long long (&c)[kDigits]) {
+    if (c[kDigits - 1] >> 63) return __longlong_as_double(0x7ff0000000000000ll);
+    uint32_t dig[kDigits];
+    unsigned long long carry = 0;
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i) {
+        const unsigned long long v = c[i] + carry;
+        dig[i] = uint32_t(v);
+        carry = v >> 32;
+    }
+    int top = -1;
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i)
+        if (dig[i]) top = i;
+    if (top < 0) return 0.0;
+    // 96 bits from the top digit down, then the rest as a sticky bit
+    const unsigned long long hi =
+        (static_cast<unsigned long long>(dig[top]) << 32) | (top >= 1 ? dig[top - 1] : 0u);
+    const uint32_t lo = top >= 2 ? dig[top - 2] : 0u;
+    bool rest = false;
+#pragma unroll
+    for (int i = 0; i < kDigits; ++i)
+        if (i < top - 2 && dig[i]) rest = true;
+    const int lz = __clzll(static_cast<long long>(hi));  // < 32: the top digit is not zero
+    const unsigned long long mm = lz ? (hi << lz) | (static_cast<unsigned long long>(lo) >> (32 - lz)) : hi;
+    rest = rest || (lz ? uint32_t(lo << lz) != 0u : lo != 0u);
+    unsigned long long keep = mm >> 11;
+    const unsigned long long drop = mm & 0x7ffu;
+    const bool up = drop > 0x400u || (drop == 0x400u && (rest || (keep & 1u)));
+    keep += up ? 1u : 0u;  // 2^53 after a carry out is still exact in fp64
+    // weight of mm's bit 0 is 2^(32 (top - 1) + kDigitBase - lz); keep drops 11 bits
+    return ldexp(static_cast<double>(keep), 32 * (top - 1) + kDigitBase - lz + 11);
+}
+
+// Reads a tensor's digit counters (and returns them to zero): its exact sum of
+// squares rounded once to fp64.
+__device__ __forceinline__ double take_exact(unsigned long long *acc) {
+    unsigned long long cnt[kDigits];
+    ulonglong2 *a = reinterpret_cast<ulonglong2 *>(acc);
+#pragma unroll
+    for (int k = 0; k < kDigits / 2; ++k) {
+        const ulonglong2 x = __ldcg(&a[k]);
+        cnt[2 * k] = x.x;
+        cnt[2 * k + 1] = x.y;
+    }
+#pragma unroll
+    for (int k = 0; k < kDigits / 2; ++k) a[k] = make_ulonglong2(0ull, 0ull);
+    return exact_sum(cnt);
+}
+
+__device__ __forceinline__ uint32_t ticket_acq_rel(uint32_t *p) {
+    uint32_t old;
+    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(old) : "l"(p) : "memory");
+    return old;
 }
 
 __device__ __forceinline__ double warp_sum(double v) {
@@ -98,7 +192,7 @@ __device__ __forceinline__ double block_sum(double v, double *sh) {
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 5)
     norm_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td, int n,
                 uint32_t n_nonempty, const char *__restrict__ buf, NormWorkspace w,
                 float *__restrict__ tensor_norms, float *__restrict__ total_norm,
@@ -146,58 +240,57 @@ __global__ void __launch_bounds__(kThreads)
     const int bad = __syncthreads_or(emax == 0x7f800000u);
     const double s = chunk_sum(sf, sh);
 
-    // ---- level 2a: the last chunk of a tensor to finish sums that tensor
+    // ---- the chunk's partial into its tensor's exact accumulator, then the ticket
     const int t = c.tensor;
+    const bool one_finisher = n <= kOneFinisher;
     if (threadIdx.x == 0) {
-        w.partial[blockIdx.x] = s;
-        w.flags[blockIdx.x] = bad ? 1 : 0;
-        __threadfence();
-        const uint32_t need = uint32_t(td[t].chunk_end - td[t].chunk_begin);
-        last = (atomicAdd(&w.tickets[t], 1u) + 1u == need);
-        if (last) w.tickets[t] = 0u;  // no other CTA of this call touches it again
-    }
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
-    const int cb = td[t].chunk_begin, ce = td[t].chunk_end;
-    double ts = 0.0;
-    int tf = 0;
-    for (int i = cb + int(threadIdx.x); i < ce; i += kThreads) {
-        ts += __ldcg(&w.partial[i]);
-        tf |= __ldcg(&w.flags[i]);
-    }
-    tf = __syncthreads_or(tf);
-    ts = block_sum(ts, sh);
-    if (threadIdx.x == 0) {
-        w.tsum[t] = ts;
-        w.tflag[t] = tf;
-        if (tensor_norms) tensor_norms[t] = float(sqrt(ts));
-        if (tensor_sumsq) tensor_sumsq[t] = ts;
-        __threadfence();
-        last = (atomicAdd(&w.tickets[n], 1u) + 1u == n_nonempty);
-        if (last) w.tickets[n] = 0u;
+        if (bad) atomicOr(&w.ticket[1], 1u);
+        else if (s < 0x1p131) {
+            if (s > 0.0) add_exact(w.acc + size_t(t) * kDigits, s);  // zero adds nothing
+        } else atomicOr(&w.acc[size_t(t) * kDigits + kDigits - 1], 1ull << 63);
+        if (one_finisher) {
+            last = ticket_acq_rel(&w.ticket[0]) + 1u == gridDim.x;
+        } else {
+            // the tensor's last chunk finishes the tensor, the last tensor the group
+            last = 0;
+            const uint32_t need = uint32_t(td[t].chunk_end - td[t].chunk_begin);
+            if (ticket_acq_rel(&w.tticket[t]) + 1u == need) {
+                w.tticket[t] = 0u;
+                const double ts = take_exact(w.acc + size_t(t) * kDigits);
+                w.tsum[t] = ts;
+                if (tensor_norms) tensor_norms[t] = float(sqrt(ts));
+                if (tensor_sumsq) tensor_sumsq[t] = ts;
+                last = ticket_acq_rel(&w.ticket[0]) + 1u == n_nonempty;
+            }
+        }
     }
     __syncthreads();
     if (!last) return;
     __threadfence();
 
-    // ---- level 2b: the last tensor to finish sums all tensors (fixed order)
+    // ---- the last CTA: every tensor's sum (or the per-tensor sums already
+    // taken), the global sum in a fixed order, the flag
     double tot = 0.0;
-    int f = 0;
     for (int i = threadIdx.x; i < n; i += kThreads) {
-        if (td[i].chunk_end > td[i].chunk_begin) {
-            tot += __ldcg(&w.tsum[i]);
-            f |= __ldcg(&w.tflag[i]);
-        } else {
-            if (tensor_norms) tensor_norms[i] = 0.0f;
-            if (tensor_sumsq) tensor_sumsq[i] = 0.0;
+        double ts = 0.0;
+        if (one_finisher) {
+            ts = take_exact(w.acc + size_t(i) * kDigits);
+        } else if (td[i].chunk_end > td[i].chunk_begin) {
+            ts = __ldcg(&w.tsum[i]);
         }
+        if (one_finisher || td[i].chunk_end == td[i].chunk_begin) {
+            if (tensor_norms) tensor_norms[i] = float(sqrt(ts));
+            if (tensor_sumsq) tensor_sumsq[i] = ts;
+        }
+        tot += ts;
     }
-    f = __syncthreads_or(f);
     tot = block_sum(tot, sh);
     if (threadIdx.x == 0) {
+        const uint32_t f = __ldcg(&w.ticket[1]);
         if (total_norm) *total_norm = float(sqrt(tot));
         *nonfinite = f ? 1 : 0;
+        w.ticket[1] = 0u;
+        w.ticket[0] = 0u;
     }
 }
 
@@ -235,19 +328,15 @@ __global__ void __launch_bounds__(kThreads)
 }  // namespace
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p) {
-    const size_t nc = p->chunks.size(), n = size_t(p->n);
-    return align256(sizeof(double) * nc) + align256(sizeof(int32_t) * nc) +
-           align256(sizeof(double) * n) + align256(sizeof(int32_t) * n) +
-           align256(sizeof(uint32_t) * (n + 1));
+    const size_t n = size_t(p->n);
+    return align256(sizeof(unsigned long long) * kDigits * n) + align256(sizeof(double) * n) +
+           align256(sizeof(uint32_t) * n) + 256;
 }
 
-size_t norm_ticket_offset(const dbuf_plan_t *p) {
-    const size_t nc = p->chunks.size(), n = size_t(p->n);
-    return align256(sizeof(double) * nc) + align256(sizeof(int32_t) * nc) +
-           align256(sizeof(double) * n) + align256(sizeof(int32_t) * n);
-}
+// Every word of the workspace is a counter that must be zero when a call starts.
+size_t norm_ticket_offset(const dbuf_plan_t *) { return 0; }
 
-size_t norm_ticket_bytes(const dbuf_plan_t *p) { return sizeof(uint32_t) * (size_t(p->n) + 1); }
+size_t norm_ticket_bytes(const dbuf_plan_t *p) { return norm_workspace_bytes(p); }
 
 int launch_norm_finish(const dbuf_plan_t *p, const double *sumsq, float *tensor_norms,
                        float *total_norm, void *stream) {

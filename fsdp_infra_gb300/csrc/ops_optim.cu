@@ -1085,6 +1085,239 @@ __global__ void __launch_bounds__(kP8Threads, 1)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Pipelined 8-bit AdamW for blocks of kBigBlockElems (16384) elements, twice a
+// stage of the kernel above (128 x 128, 64 x 256 or 256 x 64 blocks).  One CTA
+// of 16 warps per SM takes one block at a time.  The block's gradients and both
+// code arrays (6 bytes per element, 96 KB) come in by three 2-D tensor-map
+// copies into one of two shared-memory buffers; the parameters are read
+// straight from HBM into registers, issued before the wait on the buffer.
+// Pass 1: every thread (8 units of 4 consecutive elements of one block row; a
+// warp covers 128 consecutive columns) dequantises, steps the moments, keeps
+// them in registers, updates its parameters and stores them (the correctly
+// rounded forms when every |m| and v of the thread lies in [2^-60, 2^60] and
+// the step's scalars allow; IEEE forms otherwise: equal results).  The block
+// maxima meet across the CTA (integer max within a warp, shared memory across
+// warps, one barrier, which also settles the CTA's verdict on the wait and
+// frees the buffer: thread 0 then issues the block after next into it).  Pass
+// 2 encodes the codes from the moments in registers and stores them.  Sixteen
+// bytes per element move, as in the kernel above; the register kernel reads
+// the gradients and codes of these blocks twice.
+// ---------------------------------------------------------------------------
+constexpr int kBigThreads = 512;
+constexpr int kBigWarps = kBigThreads / 32;
+constexpr int kBigU = int(kBigBlockElems) / 4 / kBigThreads;  // units of 4 per thread
+constexpr int kBigStageBytes = int(kBigBlockElems) * 6;       // g (fp32) + m, v codes
+constexpr int kBigStages = 2;
+
+struct BigMaps {
+    CUtensorMap map[kP8MaxTensors][3];  // g, m codes, v codes
+    int32_t tensor[kP8MaxTensors];      // slot -> tensor
+    int32_t nslots;
+};
+
+struct BigSlot {
+    int64_t buf_off, rows, cols, scale_off;
+    int qrows, qcols, nbc, lg_upr;
+};
+
+constexpr size_t kBigSmemBytes = size_t(kBigStages) * kBigStageBytes + 1024 + kBigStages * 8 +
+                                 2 * kBigWarps * 8 + kP8MaxTensors * sizeof(BigSlot);
+
+__device__ __forceinline__ void big_issue(const BigMaps &maps, const BigSlot *slots,
+                                          const P8Item &it, char *buf, uint64_t *full) {
+    const BigSlot &g = slots[it.slot];
+    const int x = it.bj0 * g.qcols, y = it.bi0 * g.qrows;
+    mbar_arrive_expect_tx(full, uint32_t(kBigStageBytes));
+    tma_load_2d(buf, &maps.map[it.slot][0], x, y, full);
+    tma_load_2d(buf + kBigBlockElems * 4, &maps.map[it.slot][1], x, y, full);
+    tma_load_2d(buf + kBigBlockElems * 5, &maps.map[it.slot][2], x, y, full);
+}
+
+__global__ void __launch_bounds__(kBigThreads, 1)
+    adamw8_big_kernel(const __grid_constant__ BigMaps maps, const P8Item *__restrict__ items,
+                      int nitems, const TensorDesc *__restrict__ td, float *__restrict__ params,
+                      uint8_t *__restrict__ mc, uint8_t *__restrict__ vc, float *__restrict__ ms,
+                      float *__restrict__ vs, const AdamParams hp, const AdamScalars hs,
+                      const float *__restrict__ total_norm, const int32_t *__restrict__ nonfinite,
+                      int32_t *__restrict__ status) {
+    extern __shared__ unsigned char smem_raw[];
+    char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                            ~uintptr_t(1023));
+    uint64_t *full = reinterpret_cast<uint64_t *>(stages + size_t(kBigStages) * kBigStageBytes);
+    float2 *red = reinterpret_cast<float2 *>(full + kBigStages);  // [2][kBigWarps]
+    BigSlot *slots = reinterpret_cast<BigSlot *>(red + 2 * kBigWarps);
+    const int tid = int(threadIdx.x), warp = tid >> 5, lane = tid & 31;
+    const int G = int(gridDim.x);
+    if (nonfinite && *nonfinite) return;  // skipped step: nothing is written
+    if (tid < maps.nslots) {
+        const TensorDesc &d = td[maps.tensor[tid]];
+        BigSlot g;
+        g.buf_off = d.buf_off;
+        g.rows = d.rows;
+        g.cols = d.cols;
+        g.scale_off = d.scale_off;
+        g.qrows = d.qrows;
+        g.qcols = d.qcols;
+        g.nbc = d.nbc;
+        g.lg_upr = __ffs(d.qcols >> 2) - 1;
+        slots[tid] = g;
+    }
+    if (tid == 0) {
+        for (int st = 0; st < kBigStages; ++st) mbar_init(&full[st], 1);
+        mbar_fence_init();
+    }
+    __syncthreads();
+    AdamScalars s = hs;
+    s.coef = clip_coef(hp, total_norm);
+    const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
+    if (mine == 0) return;
+    int issued = 0;
+    if (tid == 0)
+        for (; issued < kBigStages && issued < mine; ++issued)
+            big_issue(maps, slots, items[int(blockIdx.x) + issued * G],
+                      stages + size_t(issued) * kBigStageBytes, &full[issued]);
+
+    for (int k = 0; k < mine; ++k) {
+        const int st = k % kBigStages;
+        const P8Item it = items[int(blockIdx.x) + k * G];
+        const BigSlot &g = slots[it.slot];
+        const int64_t si = g.scale_off + int64_t(it.bi0) * g.nbc + it.bj0;
+        const float ms_old = ms[si], vs_old = vs[si];
+        const int upr = g.qcols >> 2;
+        const int64_t r0 = int64_t(it.bi0) * g.qrows;
+        const int c0 = it.bj0 * g.qcols;
+        // the thread's units u = tid + kBigThreads * i share one column and lie dr
+        // rows apart: unit i is row row0 + i * dr of the block
+        const int row0 = tid >> g.lg_upr, cu = tid & (upr - 1);
+        const int dr = kBigThreads >> g.lg_upr;
+        const int c = c0 + 4 * cu;
+        const int so0 = row0 * g.qcols + 4 * cu, dso = dr * g.qcols;
+        const int64_t e0 = g.buf_off + (r0 + row0) * g.cols + c, de = int64_t(dr) * g.cols;
+        const int64_t rleft = g.rows - (r0 + row0);  // unit i is inside the tensor if i * dr < rleft
+        const bool col_ok = c < g.cols;
+        float p[kBigU][4], m[kBigU][4], v[kBigU][4];
+        uint32_t valid = 0;  // bit i: unit i lies inside the tensor
+#pragma unroll
+        for (int i = 0; i < kBigU; ++i) {
+            if (col_ok && int64_t(i) * dr < rleft) {
+                valid |= 1u << i;
+                load_f<4, true>(params, e0 + i * de, p[i]);
+            } else {
+                p[i][0] = p[i][1] = p[i][2] = p[i][3] = 0.0f;
+            }
+        }
+        const bool got = mbar_wait_bounded(&full[st], uint32_t(k / kBigStages) & 1u);
+
+        // pass 1: the new moments (kept), the block maxima, the parameters (updated
+        // and stored unit by unit, so that a unit's parameters die as its moments
+        // are born)
+        const char *buf = stages + size_t(st) * kBigStageBytes;
+        float mamax = 0.0f, vamax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kBigU; ++i) {
+            const int so = so0 + i * dso;
+            const float4 gg = *reinterpret_cast<const float4 *>(buf + size_t(so) * 4);
+            const uint32_t cmw = *reinterpret_cast<const uint32_t *>(buf + kBigBlockElems * 4 + so);
+            const uint32_t cvw = *reinterpret_cast<const uint32_t *>(buf + kBigBlockElems * 5 + so);
+            const uint32_t xm = cmw ^ 0x80808080u;
+            const float2 om = splat(-8388736.0f), ov = splat(-8388607.0f);
+            const float2 sm = splat(ms_old), sv = splat(vs_old);
+            const float2 m01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 0), byte_float(xm, 1)), om), sm);
+            const float2 m23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(xm, 2), byte_float(xm, 3)), om), sm);
+            const float2 v01 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cvw, 0), byte_float(cvw, 1)), ov), sv);
+            const float2 v23 = __fmul2_rn(__fadd2_rn(make_float2(byte_float(cvw, 2), byte_float(cvw, 3)), ov), sv);
+            m[i][0] = m01.x; m[i][1] = m01.y; m[i][2] = m23.x; m[i][3] = m23.y;
+            v[i][0] = v01.x; v[i][1] = v01.y; v[i][2] = v23.x; v[i][3] = v23.y;
+            adam_moments2(s, gg.x, gg.y, m[i][0], m[i][1], v[i][0], v[i][1]);
+            adam_moments2(s, gg.z, gg.w, m[i][2], m[i][3], v[i][2], v[i][3]);
+            if ((valid >> i) & 1u) {
+                const float a0 = fabsf(m[i][0]), a1 = fabsf(m[i][1]);
+                const float a2 = fabsf(m[i][2]), a3 = fabsf(m[i][3]);
+                const float ma = fmax3(fmax3(0.0f, a0, a1), a2, a3);
+                const float va = fmax3(fmax3(0.0f, v[i][0], v[i][1]), v[i][2], v[i][3]);
+                mamax = fmaxf(mamax, ma);
+                vamax = fmaxf(vamax, va);
+                float lo = fmin3_nan(fmin3_nan(a0, a1, a2), a3, v[i][0]);
+                lo = fmin3_nan(fmin3_nan(lo, v[i][1], v[i][2]), v[i][3], lo);
+                // every |m| and v of the unit inside the correctly rounded forms'
+                // range (false for a NaN)
+                if (s.fast && lo >= 0x1p-60f && fmaxf(ma, va) <= 0x1p60f) {
+                    adam_param_cr2(s, p[i][0], p[i][1], m[i][0], m[i][1], v[i][0], v[i][1]);
+                    adam_param_cr2(s, p[i][2], p[i][3], m[i][2], m[i][3], v[i][2], v[i][3]);
+                } else {
+#pragma unroll
+                    for (int w = 0; w < 4; ++w) p[i][w] = adam_param(s, p[i][w], m[i][w], v[i][w]);
+                }
+                store_f<4>(params, e0 + i * de, p[i]);
+            }
+        }
+
+        // the block maxima (non-negative, NaN-free: their bits order like their
+        // values) across the CTA; the barrier also frees the buffer
+        mamax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(mamax)));
+        vamax = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(vamax)));
+        float2 *rk = red + (k & 1) * kBigWarps;
+        if (lane == 0) rk[warp] = make_float2(mamax, vamax);
+        if (__syncthreads_or(!got)) {
+            if (tid == 0) atomicExch(status, DBUF_ETIMEOUT);
+            break;
+        }
+        if (tid == 0 && k + kBigStages < mine) {
+            big_issue(maps, slots, items[int(blockIdx.x) + (k + kBigStages) * G],
+                      stages + size_t(st) * kBigStageBytes, &full[st]);
+            issued = k + kBigStages + 1;
+        }
+#pragma unroll
+        for (int w = 0; w < kBigWarps; ++w) {
+            const float2 r = rk[w];
+            mamax = fmaxf(mamax, r.x);
+            vamax = fmaxf(vamax, r.y);
+        }
+
+        // pass 2: new scales and the codes
+        const float ms_new = block_scale_cr(mamax, 127.0f, s.i127);
+        const float vs_new = __fmul_rn(vamax, 0x1p-8f);
+        const Divisor dm = make_divisor(ms_new), dv = make_divisor(vs_new);
+        const bool vzero = !(vs_new > 0.0f);
+        if (!(dm.exact || dv.exact)) {
+#pragma unroll
+            for (int i = 0; i < kBigU; ++i) {
+                uint32_t cm, cv;
+                unit_codes_fast(m[i], v[i], dm, dv, cm, cv);
+                if ((valid >> i) & 1u) {
+                    store_c<4>(mc, e0 + i * de, cm);
+                    store_c<4>(vc, e0 + i * de, cv);
+                }
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < kBigU; ++i) {
+                if (!((valid >> i) & 1u)) continue;
+                uint32_t cm = 0, cv = 0;
+#pragma unroll
+                for (int w = 0; w < 4; ++w) {
+                    cm |= encode1<DBUF_QUANT_INT8>(quot<true>(m[i][w], dm)) << (8 * w);
+                    cv |= (vzero ? 0u : v_code<true>(v[i][w], dv)) << (8 * w);
+                }
+                store_c<4>(mc, e0 + i * de, cm);
+                store_c<4>(vc, e0 + i * de, cv);
+            }
+        }
+        if (tid == 0) {
+            ms[si] = ms_new;
+            vs[si] = vs_new;
+        }
+    }
+    __syncthreads();
+    if (tid == 0) {
+        // copies of the last blocks issued may still be in flight: wait for them
+        // (bounded) before the CTA exits (blocks are issued in order)
+        for (int j = (issued > kBigStages ? issued - kBigStages : 0); j < issued; ++j)
+            (void)mbar_wait_bounded(&full[j % kBigStages], uint32_t(j / kBigStages) & 1u);
+    }
+}
+
 }  // namespace
 
 int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float *exp_avg,
@@ -1099,8 +1332,13 @@ int launch_adamw(const dbuf_plan_t *p, float *params, const float *grads, float 
 }
 
 int prepare_optim_kernels() {
-    return int(cudaFuncSetAttribute(adamw8_pipe_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    int(kP8SmemBytes)));
+    cudaError_t e = cudaFuncSetAttribute(adamw8_pipe_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kP8SmemBytes));
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(adamw8_big_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 int(kBigSmemBytes));
+    return int(e);
 }
 
 int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8_t *m_codes,
@@ -1113,7 +1351,7 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
     // (all quantised tensors otherwise).
     const uintptr_t bits = reinterpret_cast<uintptr_t>(params) | reinterpret_cast<uintptr_t>(grads) |
                            reinterpret_cast<uintptr_t>(m_codes) | reinterpret_cast<uintptr_t>(v_codes);
-    bool pipe = !p->p8_items.empty() && (bits & 15) == 0;
+    bool pipe = (!p->p8_items.empty() || !p->big_items.empty()) && (bits & 15) == 0;
     // one launch per kP8MaxTensors tensors; every map is encoded before the first
     // launch, so that a tensor the encoder rejects sends all of them to the
     // register kernel
@@ -1139,6 +1377,25 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
         }
         batches.push_back(maps);
     }
+    // the big-block tensors: gradients and both codes by tensor maps, one block a box
+    const size_t nbig = p->big_tensors.size();
+    std::vector<BigMaps> big_batches;
+    for (size_t b0 = 0; pipe && b0 < nbig; b0 += kP8MaxTensors) {
+        BigMaps maps;
+        maps.nslots = int32_t(std::min<size_t>(kP8MaxTensors, nbig - b0));
+        for (int slot = 0; pipe && slot < maps.nslots; ++slot) {
+            const int32_t t = p->big_tensors[b0 + slot];
+            maps.tensor[slot] = t;
+            const TensorDesc &d = p->tdesc[t];
+            pipe = encode_map_2d(&maps.map[slot][0], true, const_cast<float *>(grads) + d.buf_off,
+                                 d.cols, d.rows, d.qcols, d.qrows) &&
+                   encode_map_2d(&maps.map[slot][1], false, m_codes + d.buf_off, d.cols, d.rows,
+                                 d.qcols, d.qrows) &&
+                   encode_map_2d(&maps.map[slot][2], false, v_codes + d.buf_off, d.cols, d.rows,
+                                 d.qcols, d.qrows);
+        }
+        big_batches.push_back(maps);
+    }
     const size_t n_items = pipe ? p->n_opt_rest : p->opt_items.size();
     const size_t grid = p->opt_plain.size() + n_items;
     for (size_t b = 0; pipe && b < batches.size(); ++b) {
@@ -1149,6 +1406,18 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
         const int g = n < p->dev.num_sms ? n : p->dev.num_sms;
         adamw8_pipe_kernel<<<g, kP8Threads, kP8SmemBytes, st>>>(
             batches[b], p->dev.p8_items + i0, n, p->dev.tensors, params, m_codes, v_codes,
+            m_scales, v_scales, hp, host_scalars(hp), total_norm, nonfinite, p->dev.status);
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    for (size_t b = 0; pipe && b < big_batches.size(); ++b) {
+        const size_t b0 = b * kP8MaxTensors;
+        const size_t i0 = p->big_item_start[b0], i1 = p->big_item_start[b0 + big_batches[b].nslots];
+        const int n = int(i1 - i0);
+        if (n == 0) continue;
+        const int g = n < p->dev.num_sms ? n : p->dev.num_sms;
+        adamw8_big_kernel<<<g, kBigThreads, kBigSmemBytes, st>>>(
+            big_batches[b], p->dev.big_items + i0, n, p->dev.tensors, params, m_codes, v_codes,
             m_scales, v_scales, hp, host_scalars(hp), total_norm, nonfinite, p->dev.status);
         const cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return e;

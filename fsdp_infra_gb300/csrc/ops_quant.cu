@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
     quant_pipe_kernel(const __grid_constant__ TmaMaps maps, const TileItem *__restrict__ items,
                       int nitems, const TensorDesc *__restrict__ td, uint8_t *__restrict__ codes,
                       float *__restrict__ scales, int32_t *__restrict__ status) {
-    pdl_enter();
     extern __shared__ unsigned char smem_raw[];
     // tensor copies land at 1024-byte-aligned buffers
     char *stages = reinterpret_cast<char *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -407,22 +406,38 @@ __global__ void __launch_bounds__(kPipeThreads, 1)
         }
         mbar_fence_init();
     }
-    __syncthreads();
 
     // Group grp takes this CTA's tiles k = grp, grp + 2, ...: its t-th tile is
     // k = 2t + grp, whose halves are the group's halves 2t and 2t + 1.
     const int mine = int(blockIdx.x) < nitems ? (nitems - 1 - int(blockIdx.x)) / G + 1 : 0;
     const int ntiles = (mine - grp + 1) / 2;
-    auto issue_half = [&](int h) {  // the group's first thread: half h into buffer h % 3
-        const int t = h >> 1, e = h & 1;
-        if (t >= ntiles) return;
+    auto issue_half_of = [&](int h, const PipeTile &g) {  // half h into buffer h % 3
         const int b = grp * kPipeHalves + h % kPipeHalves;
         last[b] = h;  // before the copy, whose arrive releases it to the group
-        pipe_issue(pipe_tile(items[int(blockIdx.x) + (2 * t + grp) * G], td, codes), maps, e,
-                   stages + size_t(b) * kPipeHalfBytes, &bars[b]);
+        pipe_issue(g, maps, h & 1, stages + size_t(b) * kPipeHalfBytes, &bars[b]);
     };
-    if (gtid == 0)
-        for (int h = 0; h < kPipeHalves; ++h) issue_half(h);
+    auto issue_half = [&](int h) {  // the group's first thread
+        const int t = h >> 1;
+        if (t >= ntiles) return;
+        issue_half_of(h, pipe_tile(items[int(blockIdx.x) + (2 * t + grp) * G], td, codes));
+    };
+    // The work items and tensor descriptors are written once, at upload, so the
+    // first tiles' descriptors are read before the wait for the previous kernel;
+    // only the copies of the buffer it may have written wait.
+    PipeTile first0, first1;
+    if (gtid == 0) {
+        if (ntiles > 0) first0 = pipe_tile(items[int(blockIdx.x) + grp * G], td, codes);
+        if (ntiles > 1) first1 = pipe_tile(items[int(blockIdx.x) + (2 + grp) * G], td, codes);
+    }
+    __syncthreads();
+    pdl_enter();
+    if (gtid == 0) {
+        if (ntiles > 0) {
+            issue_half_of(0, first0);
+            issue_half_of(1, first0);
+        }
+        if (ntiles > 1) issue_half_of(2, first1);
+    }
 
     for (int t = 0; t < ntiles; ++t) {
         const int i = int(blockIdx.x) + (2 * t + grp) * G;

@@ -234,6 +234,9 @@ void build_tables(dbuf_plan_t *p) {
     p->p8_items.clear();
     p->p8_tensors.clear();
     p->p8_item_start.assign(1, 0);
+    p->big_items.clear();
+    p->big_tensors.clear();
+    p->big_item_start.assign(1, 0);
     std::vector<dbuf::OptItem> p8_opt;  // register-kernel items of p8 tensors (the fallback)
     p->state_offsets.assign(n, -1);
     int64_t s_off = 0, st_off = 0;
@@ -289,7 +292,13 @@ void build_tables(dbuf_plan_t *p) {
                                 s.cols % 16 == 0 &&
                                 d.buf_off % 16 == 0 && s.rows < (int64_t(1) << 31) &&
                                 s.cols < (int64_t(1) << 31);
-                std::vector<dbuf::OptItem> &dst = p8 ? p8_opt : p->opt_items;
+                // Blocks of kBigBlockElems (two stages) take the big-block kernel under
+                // the same alignment rules, with box dimensions of at most 256.
+                const bool big = pow2(d.qrows) && pow2(d.qcols) && be == dbuf::kBigBlockElems &&
+                                 d.qcols >= 64 && d.qcols <= 256 && d.qrows <= 256 &&
+                                 s.cols % 16 == 0 && d.buf_off % 16 == 0 &&
+                                 s.rows < (int64_t(1) << 31) && s.cols < (int64_t(1) << 31);
+                std::vector<dbuf::OptItem> &dst = (p8 || big) ? p8_opt : p->opt_items;
                 for (int64_t b = 0; b < nb; b += per)
                     dst.push_back(dbuf::OptItem{t, int32_t(b / d.nbc), int32_t(b % d.nbc),
                                                 int16_t(std::min(per, nb - b)), int16_t(lanes)});
@@ -305,6 +314,15 @@ void build_tables(dbuf_plan_t *p) {
                             p->p8_items.push_back(
                                 dbuf::P8Item{slot, t, int32_t(bi), int32_t(bj)});
                     p->p8_item_start.push_back(p->p8_items.size());
+                }
+                if (big) {
+                    const int32_t slot = int32_t(p->big_tensors.size() % dbuf::kP8MaxTensors);
+                    p->big_tensors.push_back(t);
+                    for (int64_t bi = 0; bi < nbr; ++bi)
+                        for (int64_t bj = 0; bj < d.nbc; ++bj)
+                            p->big_items.push_back(
+                                dbuf::P8Item{slot, t, int32_t(bi), int32_t(bj)});
+                    p->big_item_start.push_back(p->big_items.size());
                 }
             }
             if (d.qrows == 1) {
@@ -435,7 +453,8 @@ extern "C" int dbuf_plan(const dbuf_tensor_spec *specs, int32_t n, int32_t m,
         if (p->chunks.size() > size_t(INT32_MAX) || p->tile_items.size() > size_t(INT32_MAX) ||
             p->row_items.size() > size_t(INT32_MAX) || p->pipe_items.size() > size_t(INT32_MAX) ||
             p->opt_items.size() + p->opt_plain.size() > size_t(INT32_MAX) ||
-            p->pieces.size() > size_t(INT32_MAX) || p->p8_items.size() > size_t(INT32_MAX)) {
+            p->pieces.size() > size_t(INT32_MAX) || p->p8_items.size() > size_t(INT32_MAX) ||
+            p->big_items.size() > size_t(INT32_MAX)) {
             delete p;
             return DBUF_ERANGE;
         }
@@ -518,6 +537,7 @@ extern "C" int dbuf_plan_slice(const dbuf_plan_t *p, int32_t k, dbuf_plan_t **ou
         build_tables(s);
         if (s->chunks.size() > size_t(INT32_MAX) || s->pieces.size() > size_t(INT32_MAX) ||
             s->pipe_items.size() > size_t(INT32_MAX) || s->p8_items.size() > size_t(INT32_MAX) ||
+            s->big_items.size() > size_t(INT32_MAX) ||
             s->opt_items.size() + s->opt_plain.size() > size_t(INT32_MAX)) {
             delete s;
             return DBUF_ERANGE;

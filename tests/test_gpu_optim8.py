@@ -90,6 +90,9 @@ class Case:
                 r[32:64, 32:64] = 0.0
             if s.name == "w_rows":   # zeros among normal values (mixed units)
                 g[int(o):int(o) + s.numel:7] = 0.0
+            if s.name == "b_zero":   # one whole 128x128 block of zero gradients
+                r = g[int(o):int(o) + s.numel].reshape(s.rows, s.cols)
+                r[128:256, 0:128] = 0.0
         return g
 
     def step(self, step, clip=False, skip=False, hp=None):
@@ -277,3 +280,59 @@ def test_adamw8_more_tensors_than_one_launch_holds(dbuf_lib, oracle_lib):
     c.step(2)
     c = Case(oracle_lib, specs, 4, seed=13, shift=1)
     c.step(1)
+
+
+# Blocks of 16384 elements (128x128, 64x256, 256x64) with 16-byte rows take the
+# big-block pipelined kernel: gradients and codes staged whole, parameters read
+# directly, two passes over one block per CTA at a time.
+BIG = [
+    TensorSpec("b128", 384, 256, 128, qblock=(128, 128), quant="int8"),
+    TensorSpec("bias", 77, 1, 1),
+    TensorSpec("b_edge", 300, 208, 128, qblock=(128, 128), quant="int8"),   # ragged edges
+    TensorSpec("b64x256", 192, 512, 64, qblock=(64, 256), quant="int8"),
+    TensorSpec("b256x64", 512, 128, 256, qblock=(256, 64), quant="int8"),
+    TensorSpec("norm", 208, 1, 0, kind="norm"),
+    TensorSpec("b_zero", 384, 128, 128, qblock=(128, 128), quant="int8"),
+    TensorSpec("w_tiny", 256, 128, 128, qblock=(128, 128), quant="int8"),   # tiny values
+    TensorSpec("w_sq", 96, 64, 32, qblock=(32, 32), quant="int8"),          # the stage kernel
+]
+
+
+def test_adamw8_big_blocks_steps(dbuf_lib, oracle_lib):
+    c = Case(oracle_lib, BIG, 3, seed=21)
+    assert len(c.db.specs) == len(BIG)
+    for step, (clip, skip) in enumerate([(False, False), (True, False), (True, True),
+                                         (False, False)], start=1):
+        c.step(step, clip, skip)
+
+
+def test_adamw8_big_blocks_zero_state_and_uneven_units(dbuf_lib, oracle_lib):
+    c = Case(oracle_lib, BIG, 4, units=[2, 1, 3, 1], zero=True, seed=22)
+    c.step(1, clip=True)
+    c.step(2)
+
+
+def test_adamw8_big_blocks_unaligned_take_the_register_kernel(dbuf_lib, oracle_lib):
+    c = Case(oracle_lib, BIG, 3, seed=23, shift=1)
+    c.step(1, clip=True)
+    c.step(2)
+
+
+def test_adamw8_big_blocks_two_launches(dbuf_lib, oracle_lib):
+    """19 big-block tensors: two launches of at most 16 tensors' maps."""
+    specs = []
+    for i in range(19):
+        qb = [(128, 128), (64, 256), (256, 64)][i % 3]
+        specs.append(TensorSpec(f"w{i}", qb[0] * (1 + i % 3) + (40 if i % 4 == 1 else 0),
+                                qb[1] * (1 + i % 2), qb[0], qblock=qb, quant="int8"))
+        if i % 6 == 2:
+            specs.append(TensorSpec(f"v{i}", 33 + i, 1, 1))
+    c = Case(oracle_lib, specs, 4, seed=24)
+    c.step(1)
+    c.step(2, clip=True)
+
+
+def test_adamw8_llama_layer_128x128(dbuf_lib, oracle_lib):
+    g = adam8_group(workload("llama_layer").groups[0], (128, 128))
+    c = Case(oracle_lib, list(g.tensors), 8, seed=25)
+    c.step(3, clip=True)

@@ -161,7 +161,7 @@ def test_noalloc_norm_rejects_plans_beyond_its_scratch(dbuf_lib):
     before anything runs."""
     from fsdp_infra_gb300 import DBuffer
     d = dbuf_lib
-    db = DBuffer([(1 << 31, 1, 1)], 1).upload()
+    db = DBuffer([(1, 1, 1)] * 8200, 1).upload()  # 128 bytes of counters per tensor
     assert d.dbuf_workspace_bytes(db.handle, d.DBUF_OP_NORM_NONFINITE) > d.DBUF_NOALLOC_SCRATCH_BYTES
     small = torch.zeros(16, dtype=torch.float32, device=DEV)
     out = _outs(1)
