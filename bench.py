@@ -577,7 +577,7 @@ def run_per_config(args, device, peak):
                     "elements": st.elements, "bytes_per_step": st.bytes_per_step,
                     "grad_dtype": "bf16" if w.grad_dtype == torch.bfloat16 else "f32",
                     "l2": ("buffers larger than L2 (129 MB)" if l2 else
-                           "L2-resident small case: figures are L2 rates, not HBM"),
+                           "small case: L2-resident and launch-bound, not an HBM rate"),
                     "step": {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                              "elements_per_s": round(st.elements / (ms / 1e3), 1)},
                     "ops": ops}
