@@ -202,19 +202,17 @@ class Stack:
             ns += k["db"].n_scales
         self.op_bytes["block_quant"] = 5 * qe + 4 * ns
         self.bytes_per_step = sum(self.op_bytes.values())
-        # pack, unpack, scale_accum_zero, norm (per-chunk partials + finalise) and one
-        # quantisation launch per kind of block present (tiles, row blocks).
-        # one launch per DBuffer for each of pack_cast, unpack, scale_accum_zero
-        # and norm_nonfinite, plus the quantisation kernels: one launch per 32
-        # tile-quantised tensors (the tensor maps one launch carries) and one for
-        # row blocks
+        # per DBuffer: one launch each for pack_cast, unpack and scale_accum_zero,
+        # two for norm_nonfinite (the partials, then the finishing launch), and the
+        # quantisation kernels: one launch per 32 tile-quantised tensors (the
+        # tensor maps one launch carries) and one for row blocks
         self.launches_per_step = 0
         for d in self.dbufs:
             spec = d["kind"]["spec"]
             q = [s for s in spec.tensors if s.quant and s.numel]
             tiles = sum(1 for s in q if (s.qblock[0] or s.rows) > 1)
             rows = len(q) - tiles
-            self.launches_per_step += 4 + (tiles + 31) // 32 + (1 if rows else 0)
+            self.launches_per_step += 5 + (tiles + 31) // 32 + (1 if rows else 0)
 
     def run_op(self, op):
         """One operator alone over every DBuffer of the step, launched back to back."""

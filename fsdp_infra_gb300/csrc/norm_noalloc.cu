@@ -15,11 +15,11 @@
 // address once and caches it; later calls reuse it.  A cudaDeviceReset after
 // that first call is not supported: the cached address would be stale.
 // Each call first clears the counters its norm uses in the array (a memset on
-// the caller's stream: the per-tensor accumulators and the completion ticket,
-// which must start at zero), then runs the same norm kernel as
-// dbuf_norm_nonfinite with the array as its workspace, so a call never depends
-// on what an earlier call left behind, even one that overlapped another and
-// raced on the counters.
+// the caller's stream: the per-tensor accumulators, the flag and the ticket,
+// which must start at zero), then runs the same two norm launches as
+// dbuf_norm_nonfinite with the array as their workspace, so a call never
+// depends on what an earlier call left behind, even one that overlapped another
+// and raced on the counters.
 // All calls share the one array, so calls that overlap on the GPU (different
 // streams, or several host threads) race on it and their results are not
 // valid; the caller must serialise them.  No cudaMalloc, cudaFree or other

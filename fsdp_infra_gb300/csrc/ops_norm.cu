@@ -5,8 +5,8 @@
 // Fully Sharded Data Parallel", sharded gradient scaler and known limitations
 // (per-parameter norms need tensor boundaries, not shard boundaries).
 //
-// One launch, deterministic (the same inputs give the same bits, whatever order
-// the CTAs run in), no floating-point atomics:
+// Two launches, deterministic (the same inputs give the same bits, whatever
+// order the CTAs run in), no floating-point atomics:
 //  1. one CTA per chunk: each thread sums squares of its elements in kUnroll
 //     independent fp32 accumulators (16 terms each for a full chunk), the warp
 //     adds its 32 lanes in a fixed fp32 shuffle tree (at most about 22 roundings
@@ -24,20 +24,18 @@
 //     digits; the top digits take the carries of up to 2^31 partials.  A chunk
 //     holding an inf or NaN adds nothing and raises the flag; a partial that
 //     overflowed fp32 sets the tensor's infinity mark;
-//  3. a tensor's sum: its carries resolved, the exact sum rounded once to fp64
-//     (round to nearest even: tensor_sumsq), the square root in fp64 rounded to
-//     fp32 (tensor_norms).  Groups of up to kOneFinisher tensors: each CTA takes
-//     one acquire-release ticket on a global counter, and the launch's last CTA
-//     finishes every tensor (one load and one store of 128 bytes each), so the
-//     chain at the end of the launch is one ticket round trip and that pass.
-//     Larger groups (many small tensors): each CTA takes a ticket on its
-//     tensor's counter, the tensor's last CTA finishes that tensor and takes a
-//     ticket on the global counter, so the per-tensor work is spread over the
-//     launch.  Either way the last CTA adds the per-tensor fp64 sums in the same
-//     fixed order (strided per thread, then the CTA tree) for the global norm,
-//     writes the flag, and returns every counter to zero, so each call leaves
-//     the workspace as it found it and needs no clearing launch; both ways give
-//     the same bits.
+//  3. a second, small launch (a programmatic dependent of the first, so it is
+//     resident early and starts as soon as the first completes) finishes: one
+//     thread per tensor resolves its carries, rounds the exact sum once to fp64
+//     (round to nearest even: tensor_sumsq), takes the square root in fp64 and
+//     rounds it to fp32 (tensor_norms), and returns the counters to zero; the
+//     global sum adds the per-tensor fp64 sums in a fixed order (strided per
+//     thread, then the CTA tree; across CTAs, the last one to take a ticket
+//     adds them all), and the flag is read and cleared.  Each call leaves the
+//     workspace as it found it.
+// The CTAs of the first launch take no ticket and wait for nothing: a chain of
+// tickets at the end of a launch cost 6-11 us of a short launch, whatever its
+// size, and a ticket per CTA on one counter serialised.
 #include "common.cuh"
 
 namespace dbuf {
@@ -50,15 +48,10 @@ constexpr int kDigitBase = -224;   // weight of digit 0 is 2^kDigitBase
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Groups of at most this many tensors finish in the launch's last CTA; larger
-// groups finish each tensor in the CTA that completes it (see step 3 above).
-constexpr int kOneFinisher = 256;
-
 struct NormWorkspace {
     unsigned long long *acc;  // [n][kDigits] digit counters of each tensor's sum of squares
-    double *tsum;             // [n] each tensor's sum (per-tensor finishing)
-    uint32_t *tticket;        // [n] chunks finished per tensor (per-tensor finishing)
-    uint32_t *ticket;         // [0] CTAs (or tensors) finished, [1] non-finite flag
+    double *tsum;             // [n] each tensor's sum (a finishing launch of several CTAs)
+    uint32_t *ticket;         // [0] finishing CTAs done, [1] non-finite flag
 };
 
 NormWorkspace carve(const dbuf_plan_t *p, void *ws) {
@@ -69,8 +62,6 @@ NormWorkspace carve(const dbuf_plan_t *p, void *ws) {
     b += align256(sizeof(unsigned long long) * kDigits * n);
     w.tsum = reinterpret_cast<double *>(b);
     b += align256(sizeof(double) * n);
-    w.tticket = reinterpret_cast<uint32_t *>(b);
-    b += align256(sizeof(uint32_t) * n);
     w.ticket = reinterpret_cast<uint32_t *>(b);
     return w;
 }
@@ -193,12 +184,9 @@ __device__ __forceinline__ double block_sum(double v, double *sh) {
 
 template <int DT>
 __global__ void __launch_bounds__(kThreads, 5)
-    norm_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td, int n,
-                uint32_t n_nonempty, const char *__restrict__ buf, NormWorkspace w,
-                float *__restrict__ tensor_norms, float *__restrict__ total_norm,
-                int32_t *__restrict__ nonfinite, double *__restrict__ tensor_sumsq) {
+    norm_kernel(const Chunk *__restrict__ chunks, const TensorDesc *__restrict__ td,
+                const char *__restrict__ buf, NormWorkspace w) {
     __shared__ double sh[kWarps];
-    __shared__ int last;
     pdl_enter();
     const Chunk c = chunks[blockIdx.x];
     const char *x = buf + (td[c.tensor].buf_off + c.off) * elem_bytes<DT>();
@@ -240,51 +228,46 @@ __global__ void __launch_bounds__(kThreads, 5)
     const int bad = __syncthreads_or(emax == 0x7f800000u);
     const double s = chunk_sum(sf, sh);
 
-    // ---- the chunk's partial into its tensor's exact accumulator, then the ticket
+    // ---- the chunk's partial into its tensor's exact accumulator (the
+    // finishing launch reads it)
     const int t = c.tensor;
-    const bool one_finisher = n <= kOneFinisher;
     if (threadIdx.x == 0) {
         if (bad) atomicOr(&w.ticket[1], 1u);
         else if (s < 0x1p131) {
-            if (s > 0.0) add_exact(w.acc + size_t(t) * kDigits, s);  // zero adds nothing
+            if (s > 0.0) add_exact(w.acc + size_t(t) * kDigits, s);
         } else atomicOr(&w.acc[size_t(t) * kDigits + kDigits - 1], 1ull << 63);
-        if (one_finisher) {
-            last = ticket_acq_rel(&w.ticket[0]) + 1u == gridDim.x;
-        } else {
-            // the tensor's last chunk finishes the tensor, the last tensor the group
-            last = 0;
-            const uint32_t need = uint32_t(td[t].chunk_end - td[t].chunk_begin);
-            if (ticket_acq_rel(&w.tticket[t]) + 1u == need) {
-                w.tticket[t] = 0u;
-                const double ts = take_exact(w.acc + size_t(t) * kDigits);
-                w.tsum[t] = ts;
-                if (tensor_norms) tensor_norms[t] = float(sqrt(ts));
-                if (tensor_sumsq) tensor_sumsq[t] = ts;
-                last = ticket_acq_rel(&w.ticket[0]) + 1u == n_nonempty;
-            }
-        }
     }
-    __syncthreads();
-    if (!last) return;
-    __threadfence();
+}
 
-    // ---- the last CTA: every tensor's sum (or the per-tensor sums already
-    // taken), the global sum in a fixed order, the flag
-    double tot = 0.0;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-        double ts = 0.0;
-        if (one_finisher) {
-            ts = take_exact(w.acc + size_t(i) * kDigits);
-        } else if (td[i].chunk_end > td[i].chunk_begin) {
-            ts = __ldcg(&w.tsum[i]);
-        }
-        if (one_finisher || td[i].chunk_end == td[i].chunk_begin) {
-            if (tensor_norms) tensor_norms[i] = float(sqrt(ts));
-            if (tensor_sumsq) tensor_sumsq[i] = ts;
-        }
-        tot += ts;
+// The finishing launch: CTA b finishes tensors [256 b, 256 b + 256); with more
+// than one CTA the last one (a ticket) adds the per-tensor sums in the fixed
+// order.
+__global__ void __launch_bounds__(kThreads)
+    norm_finish_exact_kernel(int n, NormWorkspace w, float *__restrict__ tensor_norms,
+                             float *__restrict__ total_norm, int32_t *__restrict__ nonfinite,
+                             double *__restrict__ tensor_sumsq) {
+    __shared__ double sh[kWarps];
+    __shared__ int last;
+    pdl_enter();
+    const int i = int(blockIdx.x) * kThreads + int(threadIdx.x);
+    double ts = 0.0;
+    if (i < n) {
+        ts = take_exact(w.acc + size_t(i) * kDigits);
+        if (tensor_norms) tensor_norms[i] = float(sqrt(ts));
+        if (tensor_sumsq) tensor_sumsq[i] = ts;
+        if (gridDim.x > 1) w.tsum[i] = ts;
     }
-    tot = block_sum(tot, sh);
+    if (gridDim.x > 1) {
+        __threadfence();  // every thread's per-tensor sum before the CTA's ticket
+        __syncthreads();
+        if (threadIdx.x == 0) last = ticket_acq_rel(&w.ticket[0]) + 1u == gridDim.x;
+        __syncthreads();
+        if (!last) return;
+        __threadfence();
+        ts = 0.0;
+        for (int j = threadIdx.x; j < n; j += kThreads) ts += __ldcg(&w.tsum[j]);
+    }
+    const double tot = block_sum(ts, sh);
     if (threadIdx.x == 0) {
         const uint32_t f = __ldcg(&w.ticket[1]);
         if (total_norm) *total_norm = float(sqrt(tot));
@@ -329,8 +312,7 @@ __global__ void __launch_bounds__(kThreads)
 
 size_t norm_workspace_bytes(const dbuf_plan_t *p) {
     const size_t n = size_t(p->n);
-    return align256(sizeof(unsigned long long) * kDigits * n) + align256(sizeof(double) * n) +
-           align256(sizeof(uint32_t) * n) + 256;
+    return align256(sizeof(unsigned long long) * kDigits * n) + align256(sizeof(double) * n) + 256;
 }
 
 // Every word of the workspace is a counter that must be zero when a call starts.
@@ -356,16 +338,18 @@ int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_nor
         return cudaGetLastError();
     }
     NormWorkspace w = carve(p, workspace);
-    uint32_t nonempty = 0;
-    for (const TensorDesc &d : p->tdesc) nonempty += d.chunk_end > d.chunk_begin ? 1u : 0u;
     const Chunk *chunks = p->dev.chunks;
     const TensorDesc *td = p->dev.tensors;
     const char *b = static_cast<const char *>(buf);
+    cudaError_t e;
     if (dt == DBUF_F32)
-        return launch_pdl(norm_kernel<DBUF_F32>, nc, kThreads, 0, st, chunks, td, p->n, nonempty, b,
-                          w, tensor_norms, total_norm, nonfinite, tensor_sumsq);
-    return launch_pdl(norm_kernel<DBUF_BF16>, nc, kThreads, 0, st, chunks, td, p->n, nonempty, b, w,
-                      tensor_norms, total_norm, nonfinite, tensor_sumsq);
+        e = launch_pdl(norm_kernel<DBUF_F32>, nc, kThreads, 0, st, chunks, td, b, w);
+    else
+        e = launch_pdl(norm_kernel<DBUF_BF16>, nc, kThreads, 0, st, chunks, td, b, w);
+    if (e != cudaSuccess) return e;
+    const unsigned fg = unsigned((p->n + kThreads - 1) / kThreads);
+    return launch_pdl(norm_finish_exact_kernel, fg, kThreads, 0, st, p->n, w, tensor_norms,
+                      total_norm, nonfinite, tensor_sumsq);
 }
 
 }  // namespace dbuf

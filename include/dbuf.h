@@ -274,15 +274,16 @@ size_t dbuf_workspace_bytes(const dbuf_plan_t *plan, int32_t op);
  * L2 norm, and a flag for any non-finite value (inf or NaN) in any tensor range.
  * [veScale OpDispatcher: ragged norm handler and non-finite check handler;
  * PyTorch FSDP sharded gradient scaler and known limitations.]
- * One launch: sums of squares are formed per chunk (fp32 lanes, fp64 across
+ * Two launches: sums of squares are formed per chunk (fp32 lanes, fp64 across
  * warps, in a fixed order) and added exactly into each tensor's fixed-point
  * accumulator (integer digits, so the order in which chunks finish does not
- * matter); the last CTA rounds each tensor's exact sum once to fp64, takes the
- * square roots in fp64 and adds the per-tensor sums in a fixed order for the
- * global norm.  Results are deterministic, run to run; norms are returned in
- * fp32.  The workspace (about 140 bytes per tensor plus 256) holds counters
- * that must be zero when a call starts: zero-fill it once after allocating it
- * (e.g. cudaMemset); every call returns them to zero before it finishes.
+ * matter); a small second launch, chained as a programmatic dependent, rounds
+ * each tensor's exact sum once to fp64, takes the square roots in fp64 and
+ * adds the per-tensor sums in a fixed order for the global norm.  Results are
+ * deterministic, run to run; norms are returned in fp32.  The workspace (136
+ * bytes per tensor plus 256) holds counters that must be zero when a call
+ * starts: zero-fill it once after allocating it (e.g. cudaMemset); every call
+ * returns them to zero before it finishes.
  * buf: device buffer of dtype (DBUF_F32 or DBUF_BF16).  Outputs are device
  * pointers: tensor_norms [n] floats, total_norm 1 float, nonfinite 1 int32
  * (0 or 1).  When the flag is 1 the norms are not meaningful.
@@ -357,8 +358,8 @@ int dbuf_block_quant(const dbuf_plan_t *plan, const float *buf, uint8_t *codes, 
  * Scratch: a static device array of DBUF_NOALLOC_SCRATCH_BYTES inside the
  * library, held by every device that loads it until the process exits.  A plan
  * whose norm needs more (dbuf_workspace_bytes(plan, DBUF_OP_NORM_NONFINITE) >
- * DBUF_NOALLOC_SCRATCH_BYTES: more than about 7,480 tensors; the element count
- * does not matter) is rejected with DBUF_ERANGE before anything is launched.  The first call on a
+ * DBUF_NOALLOC_SCRATCH_BYTES: more than 7708 tensors; the element count does
+ * not matter) is rejected with DBUF_ERANGE before anything is launched.  The first call on a
  * device looks up the array's device address (once per device, with that
  * device current) and keeps it; make that first call before any stream
  * capture, and do not reset the device (cudaDeviceReset) afterwards, since the
