@@ -1091,7 +1091,8 @@ __global__ void __launch_bounds__(kP8Threads, 1)
 // of 16 warps per SM takes one block at a time.  The block's gradients and both
 // code arrays (6 bytes per element, 96 KB) come in by three 2-D tensor-map
 // copies into one of two shared-memory buffers; the parameters are read
-// straight from HBM into registers, issued before the wait on the buffer.
+// straight into registers, issued before the wait on the buffer, from L2, where
+// a tensor-map prefetch issued with the block's copies has brought them.
 // Pass 1: every thread (8 units of 4 consecutive elements of one block row; a
 // warp covers 128 consecutive columns) dequantises, steps the moments, keeps
 // them in registers, updates its parameters and stores them (the correctly
@@ -1111,7 +1112,7 @@ constexpr int kBigStageBytes = int(kBigBlockElems) * 6;       // g (fp32) + m, v
 constexpr int kBigStages = 2;
 
 struct BigMaps {
-    CUtensorMap map[kP8MaxTensors][3];  // g, m codes, v codes
+    CUtensorMap map[kP8MaxTensors][4];  // g, m codes, v codes; p (prefetched into L2)
     int32_t tensor[kP8MaxTensors];      // slot -> tensor
     int32_t nslots;
 };
@@ -1132,6 +1133,9 @@ __device__ __forceinline__ void big_issue(const BigMaps &maps, const BigSlot *sl
     tma_load_2d(buf, &maps.map[it.slot][0], x, y, full);
     tma_load_2d(buf + kBigBlockElems * 4, &maps.map[it.slot][1], x, y, full);
     tma_load_2d(buf + kBigBlockElems * 5, &maps.map[it.slot][2], x, y, full);
+    // the block's parameters are read directly from global memory when its turn
+    // comes; bringing them into L2 now takes DRAM latency off that first read
+    tma_prefetch_l2_2d(&maps.map[it.slot][3], x, y);
 }
 
 __global__ void __launch_bounds__(kBigThreads, 1)
@@ -1377,7 +1381,8 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
         }
         batches.push_back(maps);
     }
-    // the big-block tensors: gradients and both codes by tensor maps, one block a box
+    // the big-block tensors: gradients and both codes by tensor maps, one block a
+    // box, and the parameters' map for the L2 prefetch
     const size_t nbig = p->big_tensors.size();
     std::vector<BigMaps> big_batches;
     for (size_t b0 = 0; pipe && b0 < nbig; b0 += kP8MaxTensors) {
@@ -1392,6 +1397,8 @@ int launch_adamw8(const dbuf_plan_t *p, float *params, const float *grads, uint8
                    encode_map_2d(&maps.map[slot][1], false, m_codes + d.buf_off, d.cols, d.rows,
                                  d.qcols, d.qrows) &&
                    encode_map_2d(&maps.map[slot][2], false, v_codes + d.buf_off, d.cols, d.rows,
+                                 d.qcols, d.qrows) &&
+                   encode_map_2d(&maps.map[slot][3], true, params + d.buf_off, d.cols, d.rows,
                                  d.qcols, d.qrows);
         }
         big_batches.push_back(maps);

@@ -75,6 +75,14 @@ __device__ __forceinline__ void tma_load_2d(void *smem_dst, const CUtensorMap *m
         : "memory");
 }
 
+// Prefetches the box of tensor map `map` at (x = column, y = row) into L2: no
+// shared memory, no barrier, nothing to wait for.
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
 
 // OR of `pred` over the `count` threads of named barrier `id` (a block group).
 __device__ __forceinline__ bool group_any(bool pred, int id, int count) {

@@ -77,7 +77,8 @@ def case_llama_step(dev, reps):
         db8.adamw8_step(p8, gg8, st8, step=r + 1, lr=1e-4, betas=(0.9, 0.95), weight_decay=0.1)
         db.gather(shards, mats)
         db.scatter(mats, shards)
-    return f"llama_step: {reps} reps of 9 launches on {sum(db.numel)} elements"
+    return (f"llama_step: {reps} reps of the five step operators, AdamW, 8-bit AdamW, gather and "
+            f"scatter on {sum(db.numel)} elements")
 
 
 def case_quant_row(dev, reps):
