@@ -1092,7 +1092,9 @@ __global__ void __launch_bounds__(kP8Threads, 1)
 // code arrays (6 bytes per element, 96 KB) come in by three 2-D tensor-map
 // copies into one of two shared-memory buffers; the parameters are read
 // straight into registers, issued before the wait on the buffer, from L2, where
-// a tensor-map prefetch issued with the block's copies has brought them.
+// a tensor-map prefetch issued with the block's copies has brought them.  The
+// boxes of the block after are prefetched into L2 at the same time, so that its
+// copies, issued one block later, land from L2.
 // Pass 1: every thread (8 units of 4 consecutive elements of one block row; a
 // warp covers 128 consecutive columns) dequantises, steps the moments, keeps
 // them in registers, updates its parameters and stores them (the correctly
@@ -1138,6 +1140,16 @@ __device__ __forceinline__ void big_issue(const BigMaps &maps, const BigSlot *sl
     tma_prefetch_l2_2d(&maps.map[it.slot][3], x, y);
 }
 
+// The boxes of the block issued after `it` into L2 (its copies come one block
+// later and find them there).
+__device__ __forceinline__ void big_prefetch(const BigMaps &maps, const BigSlot *slots,
+                                             const P8Item &it) {
+    const BigSlot &g = slots[it.slot];
+    const int x = it.bj0 * g.qcols, y = it.bi0 * g.qrows;
+#pragma unroll
+    for (int a = 0; a < 3; ++a) tma_prefetch_l2_2d(&maps.map[it.slot][a], x, y);
+}
+
 __global__ void __launch_bounds__(kBigThreads, 1)
     adamw8_big_kernel(const __grid_constant__ BigMaps maps, const P8Item *__restrict__ items,
                       int nitems, const TensorDesc *__restrict__ td, float *__restrict__ params,
@@ -1181,6 +1193,7 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         for (; issued < kBigStages && issued < mine; ++issued)
             big_issue(maps, slots, items[int(blockIdx.x) + issued * G],
                       stages + size_t(issued) * kBigStageBytes, &full[issued]);
+    if (tid == 0 && issued < mine) big_prefetch(maps, slots, items[int(blockIdx.x) + issued * G]);
 
     for (int k = 0; k < mine; ++k) {
         const int st = k % kBigStages;
@@ -1270,6 +1283,8 @@ __global__ void __launch_bounds__(kBigThreads, 1)
         if (tid == 0 && k + kBigStages < mine) {
             big_issue(maps, slots, items[int(blockIdx.x) + (k + kBigStages) * G],
                       stages + size_t(st) * kBigStageBytes, &full[st]);
+            if (k + kBigStages + 1 < mine)
+                big_prefetch(maps, slots, items[int(blockIdx.x) + (k + kBigStages + 1) * G]);
             issued = k + kBigStages + 1;
         }
 #pragma unroll

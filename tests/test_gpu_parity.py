@@ -417,6 +417,32 @@ def test_quant_unaligned_buffers_and_status(lib, oracle_lib):
     assert lib.dbuf_device_status(db.handle) == 0
 
 
+def test_quant_pipe_odd_block_rows(lib, oracle_lib):
+    """Blocks of the pipelined tile kernel whose row count is odd or small (each
+    half of a tile covers ceil(qrows / 2) rows, the second half one row short or
+    empty), narrow blocks, ragged tensor edges, E4M3 and INT8: codes and scales
+    bit-exact against the oracle on the whole buffer.  Every tensor qualifies
+    for the tensor-map path: block widths and row lengths multiples of 4
+    elements, offsets aligned to 16 elements."""
+    specs = []
+    for i, (qb, rows, cols) in enumerate([((7, 16), 23, 52), ((33, 64), 70, 200),
+                                          ((127, 128), 300, 260), ((3, 4), 10, 20),
+                                          ((2, 8), 9, 40), ((128, 96), 130, 100)]):
+        quant = "e4m3" if i % 2 == 0 else "int8"
+        specs.append(TensorSpec(f"w{i}", rows, cols, qb[0], qblock=qb, quant=quant))
+    db = _db(specs, 2)
+    op = oracle_lib.plan_specs(specs, 2, None, 16)
+    gen = torch.Generator().manual_seed(23)
+    host = (torch.randn(db.total, generator=gen) * 0.05).to(torch.float32)
+    want_c = np.full(db.total, 0x5A, np.uint8)
+    want_s = oracle_lib.block_quant(op, specs, host.numpy().copy(), want_c)
+    cb = torch.full((db.total,), 0x5A, dtype=torch.uint8, device=DEV)
+    codes, scales = db.block_quant(host.to(DEV), codes=cb)
+    assert_bits_equal(f32(scales), want_s, "scales")
+    assert_bits_equal(codes.cpu().numpy(), want_c, "codes")
+    assert lib.dbuf_device_status(db.handle) == 0
+
+
 def test_quant_more_tensors_than_one_launch_holds(lib, oracle_lib):
     """75 tensors of the pipelined quantisation kernel (three launches of at most
     32 tensors, block shapes 128x128, 64x128 and 32x32 in E4M3 and INT8 changing
