@@ -543,6 +543,19 @@ def step_alone_ms(stack, eager, passes=3, min_steps=32):
 
 
 PER_CONFIG = ("tiny", "llama_layer", "moe", "mixed")
+L2_BYTES = 129e6
+
+
+def l2_label(numel):
+    """How a workload's buffers sit against the 129 MB L2 (launches back to back,
+    no flush between them)."""
+    f32 = numel * 4
+    if f32 > 2 * L2_BYTES:
+        return "buffers larger than L2 (129 MB)"
+    if f32 > L2_BYTES:
+        return (f"fp32 buffers ({f32 / 1e6:.0f} MB) larger than L2 (129 MB), bf16 buffer "
+                f"({f32 / 2e6:.0f} MB) smaller: partly L2-resident between launches")
+    return "small case: L2-resident and launch-bound, not an HBM rate"
 
 
 def run_per_config(args, device, peak):
@@ -570,12 +583,10 @@ def run_per_config(args, device, peak):
                        "elements_per_s": round(st.elements / (ms / 1e3), 1)}
         ms = step_alone_ms(st, args.eager)
         gbs = st.bytes_per_step / (ms / 1e3) / 1e9
-        l2 = w.total_numel * 4 > 2 * 129e6
         out[key] = {"workload": w.description, "m": w.m, "dbuffers": len(st.dbufs),
                     "elements": st.elements, "bytes_per_step": st.bytes_per_step,
                     "grad_dtype": "bf16" if w.grad_dtype == torch.bfloat16 else "f32",
-                    "l2": ("buffers larger than L2 (129 MB)" if l2 else
-                           "small case: L2-resident and launch-bound, not an HBM rate"),
+                    "l2": l2_label(w.total_numel),
                     "step": {"ms": round(ms, 4), "gbs": round(gbs, 1), "frac": round(gbs / peak, 4),
                              "elements_per_s": round(st.elements / (ms / 1e3), 1)},
                     "ops": ops}
