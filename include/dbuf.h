@@ -301,8 +301,9 @@ int dbuf_norm_nonfinite(const dbuf_plan_t *plan, const void *buf, int32_t dtype,
 /*
  * dbuf_norm_sumsq -- the first half of a sharded norm: for each tensor (of a
  * slice plan: each piece) the sum of squares of its elements in fp64, and the
- * non-finite flag, in the same single launch and fixed order as
- * dbuf_norm_nonfinite (which takes the square roots).  The per-tensor sums of
+ * non-finite flag, from the same two launches and exact accumulation as
+ * dbuf_norm_nonfinite (whose second launch takes the square roots; here it
+ * writes each tensor's exact sum rounded once to fp64).  The per-tensor sums of
  * the m slices are then added by the caller's AllReduce and turned into norms
  * by dbuf_norm_finish.  [veScale OpDispatcher: the ragged norm handler when
  * shard and tensor boundaries differ; PyTorch FSDP known limitations: a
@@ -439,7 +440,10 @@ int dbuf_adamw_step(const dbuf_plan_t *plan, float *params, const float *grads, 
 int dbuf_plan_state_offsets(const dbuf_plan_t *plan, int64_t *state_offsets, int64_t *n_state);
 
 /*
- * dbuf_adamw8_step -- 8-bit AdamW over the group, one launch.
+ * dbuf_adamw8_step -- 8-bit AdamW over the group: a few launches, not one per
+ * tensor (the stage kernel per 16 tensors with blocks of at most 8192
+ * elements, the big-block kernel per 16 tensors with 16384-element blocks, one
+ * launch for every other tensor).
  * [veScale-FSDP §6.3 8-bit Adam: block-wise INT8 quantisation of the
  * optimizer's gradient statistics; the per-parameter block shape set through
  * orig_param_policy; blocks never cross a shard, so each shard quantises its
