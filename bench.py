@@ -25,6 +25,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import re
 import os
 import statistics
 import subprocess
@@ -769,6 +770,15 @@ def run_ours(args):
     return 0
 
 
+def _exchange_config(key, world):
+    """The workload's config with its DBuffers re-planned for `world` ranks."""
+    cfg = _config_dict(None, key)
+    desc = re.sub(r"\bm=\d+", f"m={world}", cfg["workload"])
+    desc = re.sub(r"\bs=1/\d+", f"s=1/{world}", desc)
+    cfg["workload"] = desc + "; every group re-planned evenly over the ranks for the exchange"
+    return dict(cfg, m=world, parallelism=f"fsdp{world} (one shard slice per rank)")
+
+
 def run_exchange(args):
     """--exchange: the data-parallel step with its collectives, one rank per GPU
     (fsdp_infra_gb300.exchange.ShardedStep).  Every DBuffer of the workload is
@@ -861,8 +871,7 @@ def run_exchange(args):
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
                 "higher_is_better": True, "scaling": "strong", "vs_baseline": None,
                 "dtype": "f32", "data": "synthetic", "mode": "exchange",
-                "config": dict(_config_dict(None, args.workload), m=world,
-                               parallelism=f"fsdp{world} (one shard slice per rank)"),
+                "config": _exchange_config(args.workload, world),
                 "collective_bytes_per_rank": coll, "op_bytes_per_rank": op_bytes,
                 "frac_of_peak": round(value / world / peak, 4), "peak_kind": peak_kind,
                 "launch": "eager, collectives on the default stream", "clocks": clock_info}
