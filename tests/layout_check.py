@@ -141,6 +141,25 @@ def naive_concat(specs, m, align=1):
     return S, offs, [k * S for k in range(m + 1)]
 
 
+def two_boundary_survivors(specs, sizes) -> np.ndarray:
+    """The sizes S (even shards, boundaries at k*S) that this consequence of
+    constraint (iii) leaves possible.  A tensor of n > 2S elements lies inside
+    [0, m*S] and therefore holds two consecutive boundaries k*S and (k+1)*S
+    strictly inside it; (iii) puts both a whole number of units g from its
+    start, so g divides their distance S.  Any size failing that for some
+    tensor has no layout at all.  A whole-tensor unit (g = n) never divides an
+    S < n / 2, so such a tensor always rules the size out."""
+    S = np.asarray(sizes, dtype=np.int64)
+    ok = np.ones(len(S), dtype=bool)
+    for s in specs:
+        n = s.rows * s.cols
+        if n == 0:
+            continue
+        g = max(1, min(unit_of(s.rows, s.cols, s.gran_rows), n))
+        ok &= ~((n > 2 * S) & (S % g != 0))
+    return S[ok]
+
+
 def literal_greedy(specs, U, m, units, align, window=512) -> Optional[List[int]]:
     """Greedy-leftmost offsets at unit size U by a literal scan, or None.
 
