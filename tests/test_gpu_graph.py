@@ -22,11 +22,15 @@ DEV = "cuda"
 
 
 def _ragged_quant_specs():
+    """Tensors for the three quantisers: tiles the tensor maps fetch (128x128 and
+    2x100 blocks), row blocks (1x128), and tiles they cannot (4x35: rows of 35
+    elements), between vectors and unquantised matrices."""
     from workloads.configs import TensorSpec
     return [TensorSpec("a", 256, 384, 128, qblock=(128, 128), quant="e4m3"),
             TensorSpec("v", 1000, 1, 1),
             TensorSpec("b", 200, 136, 8, qblock=(1, 128), quant="int8"),
             TensorSpec("c", 130, 100, 2, qblock=(2, 100), quant="e4m3"),
+            TensorSpec("d", 60, 70, 4, qblock=(4, 35), quant="int8"),  # the register-tile kernel
             TensorSpec("w", 77, 64, 1)]
 
 
