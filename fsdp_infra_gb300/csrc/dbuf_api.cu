@@ -145,7 +145,7 @@ extern "C" int dbuf_pack_cast(const dbuf_plan_t *p, const void *const *src, int3
     int rc = check_plan(p);
     if (rc) return rc;
     if (!dtype_ok(src_dtype) || !dtype_ok(buf_dtype)) return DBUF_EINVAL;
-    if (p->n > 0 && (!src || !buf)) return DBUF_EINVAL;
+    if ((p->n > 0 && !src) || (p->total > 0 && !buf)) return DBUF_EINVAL;
     return finish(dbuf::launch_pack(p, src, src_dtype, buf, buf_dtype, stream));
 }
 
@@ -154,7 +154,7 @@ extern "C" int dbuf_unpack(const dbuf_plan_t *p, const void *buf, int32_t buf_dt
     int rc = check_plan(p);
     if (rc) return rc;
     if (!dtype_ok(buf_dtype) || !dtype_ok(dst_dtype)) return DBUF_EINVAL;
-    if (p->n > 0 && (!dst || !buf)) return DBUF_EINVAL;
+    if ((p->n > 0 && !dst) || (p->total > 0 && !buf)) return DBUF_EINVAL;
     return finish(dbuf::launch_unpack(p, buf, buf_dtype, dst, dst_dtype, stream));
 }
 
@@ -163,7 +163,7 @@ extern "C" int dbuf_scale_accum_zero(const dbuf_plan_t *p, void *grad, int32_t g
     int rc = check_plan(p);
     if (rc) return rc;
     if (!dtype_ok(grad_dtype)) return DBUF_EINVAL;
-    if (p->n > 0 && (!grad || !acc)) return DBUF_EINVAL;
+    if (p->total > 0 && (!grad || !acc)) return DBUF_EINVAL;
     return finish(dbuf::launch_sac(p, grad, grad_dtype, acc, scale, stream));
 }
 
@@ -174,7 +174,7 @@ extern "C" int dbuf_norm_nonfinite(const dbuf_plan_t *p, const void *buf, int32_
     if (rc) return rc;
     if (!dtype_ok(dtype)) return DBUF_EINVAL;
     if (!total_norm || !nonfinite || !workspace) return DBUF_EINVAL;
-    if (p->n > 0 && (!buf || !tensor_norms)) return DBUF_EINVAL;
+    if ((p->n > 0 && !tensor_norms) || (p->total > 0 && !buf)) return DBUF_EINVAL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DBUF_EINVAL;
     if (workspace_bytes < dbuf::norm_workspace_bytes(p)) return DBUF_EINVAL;
     return finish(dbuf::launch_norm(p, buf, dtype, tensor_norms, total_norm, nonfinite, workspace,
@@ -188,7 +188,7 @@ extern "C" int dbuf_norm_sumsq(const dbuf_plan_t *p, const void *buf, int32_t dt
     if (rc) return rc;
     if (!dtype_ok(dtype)) return DBUF_EINVAL;
     if (!nonfinite || !workspace) return DBUF_EINVAL;
-    if (p->n > 0 && (!buf || !tensor_sumsq)) return DBUF_EINVAL;
+    if ((p->n > 0 && !tensor_sumsq) || (p->total > 0 && !buf)) return DBUF_EINVAL;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DBUF_EINVAL;
     if (workspace_bytes < dbuf::norm_workspace_bytes(p)) return DBUF_EINVAL;
     return finish(dbuf::launch_norm(p, buf, dtype, nullptr, nullptr, nonfinite, workspace, stream,
@@ -248,7 +248,7 @@ extern "C" int dbuf_adamw_step(const dbuf_plan_t *p, float *params, const float 
     if (!p || !hp || !dbuf::adam_params(*hp, &ap)) return DBUF_EINVAL;
     int rc = check_plan(p);
     if (rc) return rc;
-    if (p->n > 0 && (!params || !grads || !exp_avg || !exp_avg_sq)) return DBUF_EINVAL;
+    if (p->total > 0 && (!params || !grads || !exp_avg || !exp_avg_sq)) return DBUF_EINVAL;
     return finish(dbuf::launch_adamw(p, params, grads, exp_avg, exp_avg_sq, ap, total_norm,
                                      nonfinite, stream));
 }
@@ -263,7 +263,7 @@ extern "C" int dbuf_adamw8_step(const dbuf_plan_t *p, float *params, const float
     if (!p || !hp || !dbuf::adam_params(*hp, &ap)) return DBUF_EINVAL;
     int rc = check_plan(p);
     if (rc) return rc;
-    if (p->n > 0 && (!params || !grads)) return DBUF_EINVAL;
+    if (p->total > 0 && (!params || !grads)) return DBUF_EINVAL;
     if (p->n_scales > 0 &&
         (!exp_avg_codes || !exp_avg_sq_codes || !exp_avg_scales || !exp_avg_sq_scales))
         return DBUF_EINVAL;

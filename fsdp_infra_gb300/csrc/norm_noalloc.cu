@@ -64,7 +64,7 @@ extern "C" int dbuf_norm_nonfinite_noalloc(const dbuf_plan_t *p, const void *buf
     if (!p->uploaded) return DBUF_ENOTUPLOADED;
     if (dtype != DBUF_F32 && dtype != DBUF_BF16) return DBUF_EINVAL;
     if (!total_norm || !nonfinite) return DBUF_EINVAL;
-    if (p->n > 0 && (!buf || !tensor_norms)) return DBUF_EINVAL;
+    if ((p->n > 0 && !tensor_norms) || (p->total > 0 && !buf)) return DBUF_EINVAL;
     if (dbuf::norm_workspace_bytes(p) > kScratchBytes) return DBUF_ERANGE;
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);

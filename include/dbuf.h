@@ -37,6 +37,9 @@
  *    its operators must be called with that device current (else DBUF_EDEVICE).
  *  - Pointers: device pointers should be 16-byte aligned; a chunk whose source
  *    or destination is not takes a slower scalar path with identical results.
+ *    A flat buffer may be NULL when the plan's total is 0 (every tensor empty):
+ *    nothing is read or written there; per-tensor outputs and pointer tables
+ *    are still required when the plan has tensors.
  *  - Errors: 0 = DBUF_OK, negative = error code (see below).  No exception or
  *    abort crosses the ABI.  A failed kernel launch returns DBUF_ECUDA and the
  *    cudaError_t is kept for dbuf_last_cuda_error() (per host thread).

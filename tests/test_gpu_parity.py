@@ -296,6 +296,36 @@ def test_empty_group(lib):
     assert tot.item() == 0.0 and flag.item() == 0
 
 
+def test_group_of_empty_tensors(lib, oracle_lib):
+    """Tensors that all have no element (a plan of total 0, flat buffers of no
+    element, whose device pointers are NULL): every operator accepts the call,
+    touches nothing, and the norms are zero with the flag clear."""
+    specs = [TensorSpec("q", 0, 158, 1, qblock=(1, 128), quant="e4m3"),
+             TensorSpec("v", 0, 1, 1), TensorSpec("t", 0, 10, 5, qblock=(5, 4), quant="int8")]
+    for m, units in ((8, None), (4, [4, 1, 4, 3])):
+        db = _db(specs, m, units, 1)
+        assert db.total == 0
+        empty = torch.zeros(0, dtype=torch.float32, device=DEV)
+        e16 = torch.zeros(0, dtype=torch.bfloat16, device=DEV)
+        users = [torch.zeros(s.rows, s.cols, dtype=torch.float32, device=DEV) for s in specs]
+        db.pack_cast(users, e16)
+        db.unpack(e16, users)
+        db.scale_accum_zero(empty, empty, 0.5)
+        norms, tot, flag = db.norm_nonfinite(empty)
+        assert norms[:3].tolist() == [0.0, 0.0, 0.0] and tot.item() == 0.0 and flag.item() == 0
+        codes, scales = db.block_quant(empty, codes=torch.zeros(0, dtype=torch.uint8, device=DEV))
+        assert codes.numel() == 0 and scales.numel() == 0
+        db.adamw_step(empty, empty, empty, empty, step=1, lr=1e-3)
+        db.adamw8_step(empty, empty, db.new_adamw8_state(), step=1, lr=1e-3)
+        shards = [torch.zeros(0, dtype=torch.float32, device=DEV) for _ in range(m)]
+        mats = [torch.zeros(0, dtype=torch.float32, device=DEV) for _ in specs]
+        db.gather(shards, mats)
+        db.scatter(mats, shards)
+        from fsdp_infra_gb300 import dbuf
+        assert dbuf.dbuf_device_status(db.handle) == 0
+        db.close()
+
+
 def test_norm_is_deterministic_and_flags_nan(lib, oracle_lib):
     w = workload("tiny")
     specs = w.groups[0].tensors

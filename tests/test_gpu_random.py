@@ -7,8 +7,11 @@ whole-tensor row granularity), a shard count m in 1..9, even or uneven
 local_units, alignment 1 or 16, and fp32 or bf16 gradients; every operator runs
 on the GPU and is compared with the oracle on whole buffers (two accumulation
 steps).  The 8-bit AdamW cases draw groups the same way and take two steps
-against the oracle.  The cases are reproducible from their seed.
+against the oracle.  The cases are reproducible from their seed; the
+DBUF_RANDOM_CASES environment variable runs more seeds of both.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -21,6 +24,9 @@ from test_gpu_parity import full_group_parity
 pytestmark = pytest.mark.gpu
 
 BLOCKS = [(128, 128), (64, 128), (32, 32), (16, 16), (1, 128), (1, 64), (5, 4)]
+# DBUF_RANDOM_CASES=N widens both sweeps to N seeds (a longer soak of the same draws)
+_N = int(os.environ.get("DBUF_RANDOM_CASES", "0"))
+N_GROUPS, N_ADAMW8 = (_N, _N) if _N > 0 else (24, 10)
 
 
 def random_group(rng):
@@ -45,7 +51,7 @@ def random_group(rng):
     return specs, m, units, align
 
 
-@pytest.mark.parametrize("seed", range(24))
+@pytest.mark.parametrize("seed", range(N_GROUPS))
 def test_random_group_all_operators(dbuf_lib, oracle_lib, seed):
     rng = np.random.default_rng(1000 + seed)
     specs, m, units, align = random_group(rng)
@@ -59,7 +65,7 @@ def test_random_group_all_operators(dbuf_lib, oracle_lib, seed):
                       grad_dtype=gdt, scale=1.0 / max(m, 1), accum_steps=2)
 
 
-@pytest.mark.parametrize("seed", range(10))
+@pytest.mark.parametrize("seed", range(N_ADAMW8))
 def test_random_group_adamw8(dbuf_lib, oracle_lib, seed):
     rng = np.random.default_rng(2000 + seed)
     specs, m, units, align = random_group(rng)
