@@ -11,11 +11,14 @@ survive; user tensors written by unpack keep their sentinel outside the slice's
 piece.  Checked for every slice k of: the tiny two-layer group (E4M3 128x128,
 m=4); an MoE-like group (row-wise units, uneven local_units, bf16 gradients,
 INT8 1x128); a ragged group (odd vectors, E4M3 32x32 and INT8 4x16 blocks, an
-empty and a whole tensor, m=5, alignment 4); the Llama layer (m=8).  Per-piece
+empty and a whole tensor, m=5, alignment 4); the Llama layer (m=8); and seeded
+random groups (eight by default, DBUF_RANDOM_CASES for more).  Per-piece
 sums of squares added over the slices and finished by dbuf_norm_finish give
 the whole group's norms (1e-5).  AdamW and 8-bit AdamW (32x32 INT8 blocks) run
 on slices against the oracle's whole-buffer step.
 """
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -107,10 +110,29 @@ def _groups():
             ("llama_layer", ll.groups[0].tensors, ll.m, None, ll.align, torch.float32)]
 
 
-@pytest.mark.parametrize("case", range(4))
+def _random_groups(n):
+    """Seeded random groups of the kinds the random parity sweep draws (vectors,
+    matrices at several row granularities, E4M3/INT8 blocks from 1x64 to
+    128x128 and an odd 5x4, empty tensors, m 1..9, even or uneven units)."""
+    from test_gpu_random import random_group
+    out = []
+    for i in range(n):
+        rng = np.random.default_rng(3000 + i)
+        specs, m, units, align = random_group(rng)
+        gdt = torch.bfloat16 if rng.random() < 0.3 else torch.float32
+        out.append((f"random{i}", specs, m, units, align, gdt))
+    return out
+
+
+# DBUF_RANDOM_CASES=N runs N random groups instead of the default 8
+_NR = int(os.environ.get("DBUF_RANDOM_CASES", "0")) or 8
+
+
+@pytest.mark.parametrize("case", range(4 + _NR))
 def test_slice_operators_equal_the_whole_buffer(dbuf_lib, oracle_lib, case):
     from fsdp_infra_gb300 import DBuffer
-    name, specs, m, units, align, gdt = _groups()[case]
+    name, specs, m, units, align, gdt = (_groups() if case < 4 else _random_groups(case - 3))[
+        case if case < 4 else -1]
     op = oracle_lib.plan_specs(specs, m, units, align)
     db = DBuffer(specs, m, units, align).upload()
     assert db.offsets == [int(x) for x in op.offsets]
