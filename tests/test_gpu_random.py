@@ -8,7 +8,10 @@ local_units, alignment 1 or 16, and fp32 or bf16 gradients; every operator runs
 on the GPU and is compared with the oracle on whole buffers (two accumulation
 steps).  The 8-bit AdamW cases draw groups the same way and take two steps
 against the oracle.  The cases are reproducible from their seed; the
-DBUF_RANDOM_CASES environment variable runs more seeds of both.
+DBUF_RANDOM_CASES environment variable runs more seeds of both.  Larger groups
+(20-70 tensors of up to a few million elements, 128x96, 64x256 and 256x64
+blocks too) take every step operator and two 8-bit AdamW steps
+(DBUF_LARGE_RANDOM seeds, two by default).
 """
 import os
 
@@ -71,5 +74,49 @@ def test_random_group_adamw8(dbuf_lib, oracle_lib, seed):
     specs, m, units, align = random_group(rng)
     c = Case(oracle_lib, specs, m, units=units, align=align, seed=seed,
              shift=1 if rng.random() < 0.2 else 0)
+    c.step(1, clip=True)
+    c.step(2)
+
+
+# larger groups: many tensors (several quantiser and 8-bit AdamW launches),
+# tiles enough for the persistent kernels' cut grids and several rounds
+BIG_BLOCKS = [(128, 128), (64, 128), (32, 32), (1, 128), (128, 96), (64, 256), (256, 64)]
+N_LARGE = int(os.environ.get("DBUF_LARGE_RANDOM", "0")) or 2
+
+
+def large_random_group(rng):
+    specs = []
+    for t in range(int(rng.integers(20, 70))):
+        kind = rng.random()
+        if kind < 0.15:
+            specs.append(TensorSpec(f"v{t}", int(rng.integers(1, 20000)), 1, 1))
+        elif kind < 0.3:
+            rows, cols = int(rng.integers(1, 1500)), 4 * int(rng.integers(1, 400))
+            specs.append(TensorSpec(f"m{t}", rows, cols, [1, 8, rows][int(rng.integers(0, 3))]))
+        else:
+            qb = BIG_BLOCKS[int(rng.integers(0, len(BIG_BLOCKS)))]
+            rows = int(rng.integers(1, 12)) * qb[0] + int(rng.integers(0, 3)) * 7
+            cols = int(rng.integers(1, 10)) * qb[1] + int(rng.integers(0, 2)) * 20
+            quant = "e4m3" if rng.random() < 0.5 else "int8"
+            specs.append(TensorSpec(f"q{t}", rows, cols, qb[0], qblock=qb, quant=quant))
+    m = int(rng.integers(2, 17))
+    units = [int(u) for u in rng.integers(1, 4, m)] if rng.random() < 0.3 else None
+    return specs, m, units, 16
+
+
+@pytest.mark.parametrize("seed", range(N_LARGE))
+def test_large_random_group_all_operators_and_adamw8(dbuf_lib, oracle_lib, seed):
+    """Groups of 20-70 tensors up to a few million elements each: every step
+    operator on whole buffers, then two 8-bit AdamW steps, against the oracle."""
+    rng = np.random.default_rng(4000 + seed)
+    specs, m, units, align = large_random_group(rng)
+    gen = torch.Generator().manual_seed(4000 + seed)
+    params = [torch.randn(s.rows, s.cols, generator=gen) * 0.02 for s in specs]
+    full_group_parity(oracle_lib, specs, m, units, align,
+                      param_fn=lambda t: params[t],
+                      grad_fn=lambda t, step: torch.randn(specs[t].rows, specs[t].cols,
+                                                          generator=gen) * 1e-3,
+                      grad_dtype=torch.float32, scale=1.0 / m, accum_steps=1)
+    c = Case(oracle_lib, specs, m, units=units, align=align, seed=seed)
     c.step(1, clip=True)
     c.step(2)
