@@ -1,7 +1,8 @@
 """GPU parity of the whole-matrix gather and scatter (dbuf_gather /
 dbuf_scatter) against the oracle, bit for bit: m separate shard buffers, fp32
 and bf16, uneven local_units, tensors spanning several shards, skipped
-tensors, unaligned shard buffers (the element path); and at full size (a 7B
+tensors, unaligned shard buffers (the element path), 1024 shards (a tensor
+over ~960 of them); and at full size (a 7B
 layer over 64 shards) the property that holds at any size: with the shards
 cut from one flat buffer, each gathered matrix is the tensor's flat range and
 a scattered matrix lands there."""
@@ -44,7 +45,7 @@ SPECS_WHOLE = [TensorSpec("w", 200, 250, 200), TensorSpec("v", 100, 1, 1),
 @pytest.mark.parametrize("dt", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("which,m,units,shift", [("mixed", 4, None, 0), ("mixed", 7, None, 1),
                                                  ("mixed", 5, [1, 3, 2, 1, 4], 0),
-                                                 ("whole", 16, None, 0)])
+                                                 ("whole", 16, None, 0), ("mixed", 1024, None, 0)])
 def test_gather_scatter_match_oracle(dbuf_lib, oracle_lib, dt, which, m, units, shift):
     from fsdp_infra_gb300 import DBuffer
     SPECS_ = SPECS if which == "mixed" else SPECS_WHOLE

@@ -135,6 +135,16 @@ def test_tiny_transformer_group(lib, oracle_lib):
                       param_fn=pf, grad_fn=gf, grad_dtype=w.grad_dtype, scale=w.scale)
 
 
+@pytest.mark.parametrize("m", [64, 1024])
+def test_tiny_group_at_high_shard_counts(lib, oracle_lib, m):
+    """The tiny group over 64 and 1024 shards (most of them padding only): every
+    operator on whole buffers against the oracle."""
+    w = workload("tiny")
+    pf, gf = _workload_fns(w)
+    full_group_parity(oracle_lib, w.groups[0].tensors, m, None, w.align,
+                      param_fn=pf, grad_fn=gf, grad_dtype=w.grad_dtype, scale=1.0 / m)
+
+
 def test_llama_layer_accumulation(lib, oracle_lib):
     w = workload("llama_layer")
     pf, gf = _workload_fns(w)
