@@ -107,16 +107,19 @@ def large_random_group(rng):
 @pytest.mark.parametrize("seed", range(N_LARGE))
 def test_large_random_group_all_operators_and_adamw8(dbuf_lib, oracle_lib, seed):
     """Groups of 20-70 tensors up to a few million elements each: every step
-    operator on whole buffers, then two 8-bit AdamW steps, against the oracle."""
+    operator on whole buffers (fp32 or bf16 gradients), then two 8-bit AdamW
+    steps (now and then on unaligned buffers), against the oracle."""
     rng = np.random.default_rng(4000 + seed)
     specs, m, units, align = large_random_group(rng)
+    gdt = torch.bfloat16 if rng.random() < 0.3 else torch.float32
+    shift = 1 if rng.random() < 0.2 else 0  # 8-bit AdamW on unaligned buffers
     gen = torch.Generator().manual_seed(4000 + seed)
     params = [torch.randn(s.rows, s.cols, generator=gen) * 0.02 for s in specs]
     full_group_parity(oracle_lib, specs, m, units, align,
                       param_fn=lambda t: params[t],
-                      grad_fn=lambda t, step: torch.randn(specs[t].rows, specs[t].cols,
-                                                          generator=gen) * 1e-3,
-                      grad_dtype=torch.float32, scale=1.0 / m, accum_steps=1)
-    c = Case(oracle_lib, specs, m, units=units, align=align, seed=seed)
+                      grad_fn=lambda t, step: (torch.randn(specs[t].rows, specs[t].cols,
+                                                           generator=gen) * 1e-3).to(gdt),
+                      grad_dtype=gdt, scale=1.0 / m, accum_steps=1)
+    c = Case(oracle_lib, specs, m, units=units, align=align, seed=seed, shift=shift)
     c.step(1, clip=True)
     c.step(2)
