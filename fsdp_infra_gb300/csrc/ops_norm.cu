@@ -25,7 +25,8 @@
 //     holding an inf or NaN adds nothing and raises the flag; a partial that
 //     overflowed fp32 sets the tensor's infinity mark;
 //  3. a second, small launch (a programmatic dependent of the first, so it is
-//     resident early and starts as soon as the first completes) finishes: one
+//     resident early and starts as soon as the first completes; one warp for
+//     up to 32 tensors, which needs no CTA barrier) finishes: one
 //     thread per tensor resolves its carries, rounds the exact sum once to fp64
 //     (round to nearest even: tensor_sumsq), takes the square root in fp64 and
 //     rounds it to fp32 (tensor_norms), and returns the counters to zero; the
@@ -241,7 +242,8 @@ __global__ void __launch_bounds__(kThreads, 5)
 
 // The finishing launch: CTA b finishes tensors [256 b, 256 b + 256); with more
 // than one CTA the last one (a ticket) adds the per-tensor sums in the fixed
-// order.
+// order.  Up to 32 tensors take one warp: its xor tree is the CTA sum's first
+// level, and the other warps would only have added zeros.
 __global__ void __launch_bounds__(kThreads)
     norm_finish_exact_kernel(int n, NormWorkspace w, float *__restrict__ tensor_norms,
                              float *__restrict__ total_norm, int32_t *__restrict__ nonfinite,
@@ -267,7 +269,9 @@ __global__ void __launch_bounds__(kThreads)
         ts = 0.0;
         for (int j = threadIdx.x; j < n; j += kThreads) ts += __ldcg(&w.tsum[j]);
     }
-    const double tot = block_sum(ts, sh);
+    // one warp when the launch has 32 threads (n <= 32): the same xor tree,
+    // without the CTA barrier (the other warps would add zeros)
+    const double tot = blockDim.x == 32 ? warp_sum(ts) : block_sum(ts, sh);
     if (threadIdx.x == 0) {
         const uint32_t f = __ldcg(&w.ticket[1]);
         if (total_norm) *total_norm = float(sqrt(tot));
@@ -348,8 +352,8 @@ int launch_norm(const dbuf_plan_t *p, const void *buf, int dt, float *tensor_nor
         e = launch_pdl(norm_kernel<DBUF_BF16>, nc, kThreads, 0, st, chunks, td, b, w);
     if (e != cudaSuccess) return e;
     const unsigned fg = unsigned((p->n + kThreads - 1) / kThreads);
-    return launch_pdl(norm_finish_exact_kernel, fg, kThreads, 0, st, p->n, w, tensor_norms,
-                      total_norm, nonfinite, tensor_sumsq);
+    return launch_pdl(norm_finish_exact_kernel, fg, p->n <= 32 ? 32 : kThreads, 0, st, p->n, w,
+                      tensor_norms, total_norm, nonfinite, tensor_sumsq);
 }
 
 }  // namespace dbuf
